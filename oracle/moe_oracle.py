@@ -1,0 +1,239 @@
+"""fp64 CPU oracle of the Mixtral sparse mixture-of-experts layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import or run this module.
+It shares no code with the CUDA library: it takes bf16 bit patterns
+(``numpy.uint16``) straight from the input generator and widens them itself.
+
+What it computes, step by step, and where each step is defined ("Mixtral of
+Experts", arXiv 2401.04088):
+
+* layer output: ``y = sum_i G(x)_i * E_i(x)`` over the n experts, and experts
+  whose gate is zero need not be evaluated (§2.1, the layer-output sum and
+  the sentence after it);
+* gate: ``G(x) = Softmax(TopK(x . W_g))`` where ``TopK`` keeps the K largest of
+  the n logits and sets the others to minus infinity (§2.1, the gating
+  definition); Mixtral uses n = 8 and K = 2 (Table 1);
+* expert: a SwiGLU feed-forward block (§2.1, the top-2 SwiGLU form of the
+  layer).  The pages do not print the SwiGLU formula; the reading used here is
+  ``E(x) = W2 (SiLU(W1 x) * (W3 x))`` with no biases, three dim x hidden
+  matrices per expert, which is the reading that reproduces the 46.7B total /
+  12.9B active parameter counts quoted for the model (the CPU tests check this
+  against Table 1 and the quoted counts).
+
+Readings where the pages are silent:
+
+* ties in TopK go to the lower expert index; slot 0 holds the larger logit;
+* the softmax runs over the K selected logits only (the others are minus
+  infinity, so their exponentials are exactly zero);
+* the routing structures are a stable counting sort of the flat assignments
+  ``t*K + k`` by expert id (tokens ascending inside each expert group);
+* the 32-layer stack applies ``x <- x + MoE(RMSNorm(x))`` with unit gain and
+  eps = 1e-5, the normalised activations rounded to bf16 (not on the pages).
+
+Precision: every input is widened exactly from bf16 to float64 and every step
+runs in float64.  ``h_bf16=True`` additionally rounds the SwiGLU activations to
+bf16 before the down projection (the rounding point of the GPU path); parity
+uses the exact mode.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------- bf16 ----
+
+def widen_bf16(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: a bf16 is the top half of a float32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def round_bf16(values) -> np.ndarray:
+    """float64 -> bf16 bit patterns, one round-to-nearest-even step.
+
+    Finite values inside the bf16 normal range (or zero) only; the oracle never
+    produces anything else.
+    """
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    bits = v.view(np.uint64)
+    # Keep sign, 11 exponent bits and 7 mantissa bits of the float64; round the
+    # 45 dropped mantissa bits to nearest, ties to even.  A mantissa carry
+    # propagates into the exponent field, as rounding requires.
+    lsb = (bits >> np.uint64(45)) & np.uint64(1)
+    r = (bits + np.uint64((1 << 44) - 1) + lsb) >> np.uint64(45)
+    sign = (r >> np.uint64(18)) & np.uint64(1)
+    exp11 = (r >> np.uint64(7)) & np.uint64(0x7FF)
+    mant = r & np.uint64(0x7F)
+    zero = (bits & np.uint64(0x7FFFFFFFFFFFFFFF)) == 0
+    exp8 = exp11.astype(np.int64) - 1023 + 127
+    ok = zero | ((exp8 >= 1) & (exp8 <= 254))
+    if not np.all(ok):
+        raise ValueError("round_bf16: value outside the bf16 normal range")
+    exp8 = np.where(zero, 0, exp8).astype(np.uint64)
+    mant = np.where(zero, np.uint64(0), mant)
+    out = (sign << np.uint64(15)) | (exp8 << np.uint64(7)) | mant
+    return out.astype(np.uint16)
+
+
+# ------------------------------------------------------------- router ----
+
+def router_logits(x, w_gate) -> np.ndarray:
+    """Logits l = x . W_g in float64 (§2.1, the gating definition).
+
+    x: [T, dim] (bf16 bits or float64), w_gate: [dim, n]; returns [T, n].
+    """
+    return _f64(x) @ _f64(w_gate)
+
+
+def topk_order(logits: np.ndarray) -> np.ndarray:
+    """Expert indices of every token ordered by (logit descending, index ascending)."""
+    # A stable sort of -l keeps equal logits in ascending index order.
+    return np.argsort(-logits, axis=1, kind="stable")
+
+
+def router(x, w_gate, top_k: int):
+    """Top-K selection and gates (§2.1, the gating definition).
+
+    Returns (ids [T, K] int64, gates [T, K] float64, logits [T, n]); slot k of
+    a token holds its k-th largest logit, ties to the lower expert index, and
+    the gates are the softmax of the K selected logits.
+    """
+    logits = router_logits(x, w_gate)
+    ids = topk_order(logits)[:, :top_k]
+    sel = np.take_along_axis(logits, ids, axis=1)
+    return ids, softmax_selected(sel), logits
+
+
+def softmax_selected(sel: np.ndarray) -> np.ndarray:
+    """Softmax over the selected logits (the masked ones contribute exp(-inf) = 0)."""
+    z = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+# ------------------------------------------------------------- expert ----
+
+def silu(a: np.ndarray) -> np.ndarray:
+    """SiLU(a) = a * sigmoid(a) = a / (1 + exp(-a))."""
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_weight_shapes(dim: int, hidden: int):
+    """Shapes of the three matrices one SwiGLU expert reads: W1, W3, W2."""
+    return [(hidden, dim), (hidden, dim), (dim, hidden)]
+
+
+def expert_hidden(xr, w1, w3, h_bf16: bool = False) -> np.ndarray:
+    """SwiGLU activations SiLU(W1 x) * (W3 x) for the rows of ``xr`` ([m, dim] -> [m, hidden])."""
+    xr, w1, w3 = _f64(xr), _f64(w1), _f64(w3)
+    assert w1.shape == w3.shape and w1.shape[1] == xr.shape[1]
+    s = silu(xr @ w1.T) * (xr @ w3.T)
+    if h_bf16:
+        s = widen_bf16(round_bf16(s))
+    return s
+
+
+def expert_ffn(xr, w1, w3, w2, h_bf16: bool = False) -> np.ndarray:
+    """E(x) = W2 (SiLU(W1 x) * (W3 x)) applied to each row of ``xr`` ([m, dim] -> [m, dim])."""
+    w2 = _f64(w2)
+    s = expert_hidden(xr, w1, w3, h_bf16)
+    assert w2.shape == (np.asarray(xr).shape[1], s.shape[1])
+    return s @ w2.T
+
+
+# ---------------------------------------------------------- the layer ----
+
+def moe_layer(x, w_gate, w1, w3, w2, top_k: int, h_bf16: bool = False):
+    """Sparse MoE layer forward (§2.1, the top-2 SwiGLU form of the layer).
+
+    x: [T, dim]; w_gate: [dim, n]; w1, w3: [n, hidden, dim]; w2: [n, dim, hidden].
+    Each token evaluates only its K selected experts (experts with a zero gate
+    are skipped).  Returns (y [T, dim] float64, ids [T, K], gates [T, K]).
+    """
+    xf = _f64(x)
+    ids, gates, _ = router(xf, w_gate, top_k)
+    T, dim = xf.shape
+    n = np.asarray(w1).shape[0]
+    y = np.zeros((T, dim))
+    for e in range(n):                      # sum over the experts in index order
+        tok, slot = np.nonzero(ids == e)
+        if len(tok) == 0:
+            continue
+        out = expert_ffn(xf[tok], w1[e], w3[e], w2[e], h_bf16)
+        y[tok] += gates[tok, slot][:, None] * out
+    return y, ids, gates
+
+
+def rmsnorm_bf16(x, eps: float) -> np.ndarray:
+    """bf16 bits of x / sqrt(mean(x^2) + eps) per row (unit gain; stack workload only)."""
+    xf = _f64(x)
+    r = np.sqrt((xf * xf).mean(axis=1, keepdims=True) + eps)
+    return round_bf16(xf / r)
+
+
+def stack_layer(x_bits, w_gate, w1, w3, w2, top_k: int, eps: float):
+    """One residual block of the stack: x + MoE(RMSNorm(x)), float64 (not bf16-rounded)."""
+    u = rmsnorm_bf16(x_bits, eps)
+    y, ids, gates = moe_layer(u, w_gate, w1, w3, w2, top_k)
+    return _f64(x_bits) + y, ids, gates, u
+
+
+# ---------------------------------------------- the layer, step by step ----
+
+def routing_tables(ids: np.ndarray, n_experts: int):
+    """Expert-grouped permutation of the flat assignments a = t*K + k.
+
+    counts[e]   number of assignments to expert e;
+    offsets     exclusive prefix sum of counts, length n + 1;
+    perm_src[r] token of the assignment stored at grouped row r (stable: tokens
+                ascending inside each expert group);
+    slot_row[a] grouped row of assignment a (the inverse permutation).
+    """
+    flat = np.asarray(ids).reshape(-1)
+    K = np.asarray(ids).shape[1]
+    counts = np.bincount(flat, minlength=n_experts).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    order = np.argsort(flat, kind="stable")      # grouped row -> flat assignment
+    perm_src = order // K
+    slot_row = np.empty_like(order)
+    slot_row[order] = np.arange(len(order))
+    return counts, offsets, perm_src, slot_row
+
+
+def grouped_ffn(x_perm, offsets, w1, w3, w2, h_bf16: bool = False):
+    """Expert FFN over grouped rows: rows [offsets[e], offsets[e+1]) use expert e.
+
+    Returns (y_perm [R, dim], hidden activations [R, hidden]), float64.
+    """
+    xp = _f64(x_perm)
+    n = len(offsets) - 1
+    hidden = np.asarray(w1).shape[1]
+    y_perm = np.zeros_like(xp)
+    hid = np.zeros((xp.shape[0], hidden))
+    for e in range(n):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            hid[lo:hi] = expert_hidden(xp[lo:hi], w1[e], w3[e], h_bf16)
+            y_perm[lo:hi] = hid[lo:hi] @ _f64(w2[e]).T
+    return y_perm, hid
+
+
+def combine(y_perm, slot_row, gates, residual=None) -> np.ndarray:
+    """y[t] = sum_k gates[t, k] * y_perm[slot_row[t*K + k]] (+ residual[t]), float64."""
+    yp = _f64(y_perm)
+    g = np.asarray(gates, dtype=np.float64)
+    T, K = g.shape
+    rows = np.asarray(slot_row).reshape(T, K)
+    y = np.zeros((T, yp.shape[1]))
+    for k in range(K):
+        y += g[:, k:k + 1] * yp[rows[:, k]]
+    if residual is not None:
+        y += _f64(residual)
+    return y
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return widen_bf16(a)
+    return a.astype(np.float64, copy=False)
