@@ -1,0 +1,444 @@
+"""Throughput of the Mixtral sparse MoE layer forward on B300 (one JSON line).
+
+A step is one pass of the whole hot path over two batches of synthetic
+Mixtral-shaped tokens (dim 4096, hidden 14336, 8 experts, top-2; Table 1 of
+"Mixtral of Experts"): a decode-sized layer call (T=16, weight-bandwidth
+bound, small-T weight-stream FFN) and a prefill-sized layer call (T=4096,
+tensor-core bound, grouped-GEMM FFN), each router -> grouping -> expert FFN ->
+combine through the C ABI on resident inputs.  value = tokens of both batches
+per second of step time.  Per-layer figures and the roofline of the dominant
+unit (the prefill expert FFN: its two tcgen05 grouped-GEMM kernels) are
+reported beside it, as is the fp64 oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the layer has
+no cross-GPU exchange here); timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at Mixtral dims (T=16/4096) + % of TC/HBM roofline"
+DECODE, PREFILL = "decode", "prefill"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_setup(ngpu):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- workload ---
+
+def load_layer(name):
+    """Generator inputs (bf16 bits) of a named workload; no gap filter (timing only)."""
+    import moe_inputs as mi
+    cfg = mi.CONFIGS[name]
+    return cfg, mi.make_layer(cfg)
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def alg_flops(cfg):
+    """Algorithmic FLOPs of one layer call: router 2dn + K experts x 6dh per token."""
+    return cfg.T * (2 * cfg.dim * cfg.n_experts + cfg.top_k * 6 * cfg.dim * cfg.hidden)
+
+
+def alg_bytes(cfg, touched):
+    """Algorithmic HBM bytes: touched experts' weights + router + x in + y out."""
+    return (touched * 3 * cfg.dim * cfg.hidden * 2 + cfg.dim * cfg.n_experts * 2
+            + 2 * cfg.T * cfg.dim * 2)
+
+
+class Buffers:
+    """Device state of one layer: weights, inputs, stepwise buffers, workspace."""
+
+    def __init__(self, cfg, L):
+        import torch
+        import sparse_mixture_experts_46_b300 as moe
+        self.cfg = cfg
+        T, K, n, d, h = cfg.T, cfg.top_k, cfg.n_experts, cfg.dim, cfg.hidden
+        R = T * K
+        self.x, self.wg, self.w1, self.w3, self.w2 = (to_dev(a) for a in (L.x, L.wg, L.w1, L.w3,
+                                                                          L.w2))
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.ids = torch.empty((T, K), **i32)
+        self.gates = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        self.counts = torch.empty((n,), **i32)
+        self.offsets = torch.empty((n + 1,), **i32)
+        self.perm_src = torch.empty((R,), **i32)
+        self.slot_row = torch.empty((R,), **i32)
+        self.x_perm = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+        self.h = torch.empty((R, h), dtype=torch.bfloat16, device="cuda")
+        self.y_perm = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+        self.y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+        self.ws = moe.new_workspace(cfg)
+        self.x_host = torch.from_numpy(np.ascontiguousarray(L.x).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        self.y_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+        self.x_e2e = torch.empty_like(self.x)
+        self.y_e2e = torch.empty_like(self.y)
+
+    def router_permute(self):
+        import sparse_mixture_experts_46_b300 as moe
+        c = self.cfg
+        moe.moe_router_topk(c, self.x, self.wg, self.ids, self.gates, self.counts)
+        moe.moe_permute(c, self.x, self.ids, self.offsets, self.perm_src, self.slot_row,
+                        self.x_perm, self.ws)
+
+    def ffn(self):
+        import sparse_mixture_experts_46_b300 as moe
+        moe.moe_expert_ffn_grouped(self.cfg, self.x_perm, self.offsets, self.w1, self.w3,
+                                   self.w2, self.h, self.y_perm, self.ws)
+
+    def combine(self):
+        import sparse_mixture_experts_46_b300 as moe
+        moe.moe_combine(self.cfg, self.y_perm, self.slot_row, self.gates, self.y)
+
+    def layer_e2e(self):
+        """Host buffers: pinned x -> device, layer forward, y -> pinned host."""
+        import sparse_mixture_experts_46_b300 as moe
+        self.x_e2e.copy_(self.x_host, non_blocking=True)
+        moe.moe_layer_forward(self.cfg, self.x_e2e, self.wg, self.w1, self.w3, self.w2,
+                              self.y_e2e, self.ws)
+        self.y_host.copy_(self.y_e2e, non_blocking=True)
+
+
+KERNELS_PER_LAYER = 8  # router, hist, scan, scatter, gather, gate/up GEMM, down GEMM, combine
+
+
+# --------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        import torch
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, AttributeError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- traffic ---
+
+def recorded_traffic():
+    """Per-launch DRAM traffic of the dominant unit from the committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "sparse_mixture_experts_46_b300", "csrc", "grouped_gemm.cu")
+    try:
+        rec = json.load(open(path))
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    if rec.get("grouped_gemm_sha") != digest:
+        return None
+    return rec.get("prefill_ffn_bytes_per_launch")
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, \
+            "fallback"
+
+
+# ------------------------------------------------------------ oracle CPU ---
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(layers, prefill_tokens):
+    """The oracle on the decode batch and a seeded sample of the prefill batch."""
+    from oracle import moe_oracle as orc
+    tokens = 0
+    t0 = time.perf_counter()
+    for name, (cfg, L) in layers.items():
+        if name == DECODE:
+            rows = np.arange(cfg.T)
+        else:
+            rows = np.sort(np.random.default_rng(1).choice(cfg.T, prefill_tokens, replace=False))
+        orc.moe_layer(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k)
+        tokens += len(rows)
+    return tokens, time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------ main ---
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    layers = {DECODE: load_layer(DECODE), PREFILL: load_layer(PREFILL)}
+    prefill_tokens = 32
+    for _ in range(args.warmup):
+        oracle_sample(layers, prefill_tokens)
+    total_tok, total_s = 0, 0.0
+    for _ in range(args.steps):
+        tok, s = oracle_sample(layers, prefill_tokens)
+        total_tok += tok
+        total_s += s
+    value = total_tok / total_s
+    sample = ("fp64 oracle per step: decode batch (16 tokens) + %d seeded prefill tokens"
+              % prefill_tokens)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(layers),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def config_block(layers):
+    dc = layers[DECODE][0]
+    return {"workload": "Mixtral-shaped MoE layer, decode batch T=16 + prefill batch T=4096 "
+                        "(dim 4096, hidden 14336, 8 experts, top-2, bf16 weights)",
+            "T": [layers[DECODE][0].T, layers[PREFILL][0].T], "dim": dc.dim,
+            "hidden": dc.hidden, "n_experts": dc.n_experts, "top_k": dc.top_k,
+            "parallelism": "replicas", "l2": "inputs larger than L2 (2.8 GB of expert "
+                                             "weights per layer, streamed every step)"}
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import torch
+    import sparse_mixture_experts_46_b300 as moe
+    layers = {DECODE: load_layer(DECODE), PREFILL: load_layer(PREFILL)}
+    bufs = {k: Buffers(cfg, L) for k, (cfg, L) in layers.items()}
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for i, name in enumerate((DECODE, PREFILL)):
+            b = bufs[name]
+            if ev is not None:
+                ev[name][0].record(stream)
+            b.router_permute()
+            if ev is not None:
+                ev[name][1].record(stream)
+            b.ffn()
+            if ev is not None:
+                ev[name][2].record(stream)
+            b.combine()
+            if ev is not None:
+                ev[name][3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for b in bufs.values():
+        st = moe.moe_check_error(b.ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device error word after warm-up: %d" % st)
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [{n: [mk() for _ in range(4)] for n in (DECODE, PREFILL)} for _ in range(args.steps)]
+    start, end = mk(), mk()
+    clocks = ClockSampler()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), world)
+    ms_step = ms_total / args.steps
+
+    def mean_ms(name, a, b):
+        return statistics.fmean(e[name][a].elapsed_time(e[name][b]) for e in evs)
+
+    per = {}
+    pk, pk_kind = peaks()
+    for name in (DECODE, PREFILL):
+        cfg = bufs[name].cfg
+        touched = int((bufs[name].counts.cpu().numpy() > 0).sum())
+        layer_ms = mean_ms(name, 0, 3)
+        ffn_ms = mean_ms(name, 1, 2)
+        R = cfg.T * cfg.top_k
+        ffn_flops = 6.0 * R * cfg.dim * cfg.hidden
+        ffn_bytes = touched * 3 * cfg.dim * cfg.hidden * 2 + 2 * R * cfg.dim * 2
+        t_roof = max(alg_flops(cfg) / (pk["bf16_tflops"] * 1e12),
+                     alg_bytes(cfg, touched) / (pk["hbm_gbs"] * 1e9))
+        per[name] = {
+            "T": cfg.T, "layer_ms": layer_ms, "tokens_per_s": cfg.T / (layer_ms * 1e-3),
+            "router_permute_ms": mean_ms(name, 0, 1), "ffn_ms": ffn_ms,
+            "combine_ms": mean_ms(name, 2, 3), "experts_touched": touched,
+            "layer_roofline_frac": t_roof / (layer_ms * 1e-3),
+            "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
+            "ffn_hbm_gbs": ffn_bytes / (ffn_ms * 1e-3) / 1e9,
+        }
+    pre = per[PREFILL]
+    dec = per[DECODE]
+    dec["roofline"] = {"bound": "hbm", "achieved": dec["ffn_hbm_gbs"], "peak": pk["hbm_gbs"],
+                       "unit": "GB/s", "frac": dec["ffn_hbm_gbs"] / pk["hbm_gbs"],
+                       "kernel": "expert FFN, weight-stream layout (2 tcgen05 kernels)",
+                       "peak_kind": pk_kind}
+
+    # end to end: pinned host x in, layer forward through the C ABI, y back to pinned host
+    for _ in range(args.warmup):
+        for name in (DECODE, PREFILL):
+            bufs[name].layer_e2e()
+    torch.cuda.synchronize()
+    e_start, e_end = mk(), mk()
+    barrier(world)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        for name in (DECODE, PREFILL):
+            bufs[name].layer_e2e()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), world) / args.steps
+    for b in bufs.values():
+        st = moe.moe_check_error(b.ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device error word after timing: %d" % st)
+
+    tokens = sum(layers[n][0].T for n in (DECODE, PREFILL))
+    io_bytes = sum(2 * layers[n][0].T * layers[n][0].dim for n in (DECODE, PREFILL))
+    result = {
+        "metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator, Table 1 shapes, random-init weights)",
+        "config": config_block(layers),
+        "roofline": {"bound": "tensor", "achieved": pre["ffn_tflops"],
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": pre["ffn_tflops"] / pk["bf16_tflops"],
+                     "traffic": recorded_traffic(), "peak_kind": pk_kind,
+                     "frac_of_sustained": pre["ffn_tflops"] / pk["bf16_tflops_sustained"],
+                     "kernel": "prefill expert FFN: gate/up + down tcgen05 grouped GEMMs, "
+                               "6*T*K*dim*hidden FLOP per launch"},
+        "layers": per,
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": KERNELS_PER_LAYER * 2 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_layers = {n: layers[n] for n in (DECODE, PREFILL)}
+        tok, secs = oracle_sample(host_layers, 32)
+        result["cpu_baseline"] = {
+            "value": tok / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "fp64 oracle: decode batch (16 tokens) + 32 seeded prefill tokens, "
+                      "%.1f s" % secs}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

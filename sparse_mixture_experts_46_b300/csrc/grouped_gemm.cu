@@ -1,0 +1,447 @@
+// grouped_gemm.cu -- expert SwiGLU FFN as two grouped GEMMs over variable-size
+// expert groups, on the 5th-generation tensor cores (tcgen05 + TMEM), fed by
+// TMA ("Mixtral of Experts" section 2.1: each selected expert is a SwiGLU
+// feed-forward block; the per-expert token groups have different sizes).
+//
+//   pass 1 (gate/up, GLU):  H[r]      = bf16(SiLU(X[r] W1_e^T) * (X[r] W3_e^T))
+//   pass 2 (down):          Y_perm[r] = bf16(H[r] W2_e^T)
+// for every grouped row r of expert e (rows [offsets[e], offsets[e+1])).
+//
+// One persistent kernel template, two operand layouts:
+//  * tokens on M (SWAP = false; large T): the MMA is 128 token rows x N weight
+//    rows.  In pass 1 the B tile stacks 128 rows of W1 over the same 128 rows
+//    of W3, so one M128xN256 MMA produces both halves of the gate in TMEM and
+//    the epilogue applies SiLU(a)*g column-pair-wise.  In pass 2 B is 256 (or
+//    128) rows of W2.
+//  * weights on M (SWAP = true; small T): the MMA is 128 weight rows x N = 32
+//    token rows, so every weight byte is streamed from HBM exactly once per
+//    32-token chunk of an expert; pass 1 issues two MMAs per K-slice (W1 and
+//    W3 tiles against the same token tile) into two TMEM accumulators.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one thread): fills a STAGES-deep shared-memory
+//               ring, one mbarrier pair (full/empty) per stage;
+//   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma per 16-wide
+//               K slice, tcgen05.commit frees the ring slot and, after the
+//               last K block, signals the accumulator;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane TMEM quarter, SwiGLU /
+//               convert, bf16 stores; double-buffered accumulators let the
+//               epilogue of tile i overlap the main loop of tile i+1.
+// Tiles are scheduled from the device-resident offsets (the host never sees
+// the per-expert counts): tile t -> expert e, weight tile wt, token tile at,
+// ordered expert-major, then weight tile, then token tile, so CTAs working at
+// the same time share weight tiles through L2.
+//
+// Every wait is bounded (device.cuh): on expiry the CTA records the error
+// word, lets its in-flight TMA copies and MMAs land, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+struct GemmArgs {
+  const int32_t* offsets;  // [n + 1] grouped-row offsets (device)
+  uint16_t* out;           // H [R, hidden] (pass 1) or y_perm [R, dim] (pass 2)
+  uint32_t* err;           // workspace error word
+  uint64_t limit_ns;       // bounded-wait limit
+  int n_experts;
+  int k_blocks;            // reduction length / 64
+  int w_tiles;             // weight tiles per expert
+  int w_rows_per_expert;   // rows of one expert's weight matrix (hidden or dim)
+  int out_ld;              // output row stride in elements
+};
+
+template <bool SWAP, bool GLU, int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int BK = 64;                                // bf16 per 128-byte row
+  static constexpr int A_BYTES = 128 * 128;                    // one 128-row operand tile
+  static constexpr int NUM_A = (SWAP && GLU) ? 2 : 1;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = (SWAP && GLU) ? 2 * BN : BN;  // fp32 columns per buffer
+  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
+                                   : (2 * ACC_COLS <= 64)  ? 64
+                                   : (2 * ACC_COLS <= 128) ? 128
+                                   : (2 * ACC_COLS <= 256) ? 256
+                                                           : 512;
+  static constexpr int ACT_ROWS = SWAP ? BN : 128;             // token rows per tile
+  static constexpr int W_ROWS = SWAP ? 128 : (GLU ? BN / 2 : BN);  // weight rows per matrix
+  static constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
+  static constexpr int AUX_BYTES = 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;  // + alignment slack
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+  static_assert(2 * ACC_COLS <= 512, "TMEM columns");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(!(!SWAP && GLU) || BN == 256, "gate/up pass stacks two 128-row weight tiles");
+};
+
+// Bounded wait that ignores the abort flag: used to let copies / MMAs that are
+// already in flight complete before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                           uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrTimeoutDrain);
+      return;
+    }
+  }
+}
+
+template <bool SWAP, bool GLU, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
+                        const __grid_constant__ CUtensorMap tm_w0,
+                        const __grid_constant__ CUtensorMap tm_w1, const GemmArgs args) {
+  using C = GemmCfg<SWAP, GLU, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* aux = tiles + STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;       // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_tile_start = abort_flag + 1;               // [kMaxExperts + 1]
+  int* s_act_tiles = s_tile_start + kMaxExperts + 1;  // [kMaxExperts]
+  int* s_off = s_act_tiles + kMaxExperts;           // [kMaxExperts + 1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n = args.n_experts;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    int acc = 0;
+    for (int e = 0; e < n; ++e) {
+      const int lo = args.offsets[e];
+      int cnt = args.offsets[e + 1] - lo;
+      if (cnt < 0) cnt = 0;
+      const int at = (cnt + C::ACT_ROWS - 1) / C::ACT_ROWS;
+      s_off[e] = lo;
+      s_act_tiles[e] = at;
+      s_tile_start[e] = acc;
+      acc += at * args.w_tiles;
+    }
+    s_off[n] = args.offsets[n];
+    s_tile_start[n] = acc;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_act);
+    tma_prefetch_desc(&tm_w0);
+    if (GLU) tma_prefetch_desc(&tm_w1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = s_tile_start[n];
+  const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
+
+  auto decode_tile = [&](int t, int& e, int& at, int& wt) {
+    e = 0;
+    while (t >= s_tile_start[e + 1]) ++e;
+    const int local = t - s_tile_start[e];
+    const int na = s_act_tiles[e];
+    wt = local / na;
+    at = local - wt * na;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer ---
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        int e, at, wt;
+        decode_tile(t, e, at, wt);
+        const int act_row = s_off[e] + at * C::ACT_ROWS;
+        const int w_row = e * args.w_rows_per_expert + wt * C::W_ROWS;
+        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          const int kx = kb * C::BK;
+          if (!SWAP) {
+            tma_load_2d(st, &tm_act, kx, act_row, &full[s]);
+            tma_load_2d(st + C::A_BYTES, &tm_w0, kx, w_row, &full[s]);
+            if (GLU) tma_load_2d(st + C::A_BYTES + (BN / 2) * 128, &tm_w1, kx, w_row, &full[s]);
+          } else {
+            tma_load_2d(st, &tm_w0, kx, w_row, &full[s]);
+            if (GLU) tma_load_2d(st + C::A_BYTES, &tm_w1, kx, w_row, &full[s]);
+            tma_load_2d(st + C::NUM_A * C::A_BYTES, &tm_act, kx, act_row, &full[s]);
+          }
+        }
+      }
+      // Let every issued copy land before the CTA can exit.
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        drain_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, args.err, args.limit_ns);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + (uint32_t)(b * C::ACC_COLS);
+        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(tiles + s * C::STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            if (!SWAP) {
+              mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + kk * 32),
+                          sdesc_kmajor_sw128(sa + C::A_BYTES + kk * 32), C::IDESC, accum);
+            } else {
+              const uint32_t sb = sa + C::NUM_A * C::A_BYTES;
+              mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
+                          C::IDESC, accum);
+              if (GLU)
+                mma_bf16_ss(d0 + BN, sdesc_kmajor_sw128(sa + C::A_BYTES + kk * 32),
+                            sdesc_kmajor_sw128(sb + kk * 32), C::IDESC, accum);
+            }
+          }
+          mma_commit(&empty[s]);  // ring slot free once these MMAs have read it
+        }
+        if (!ok) break;
+        mma_commit(&tfull[b]);    // accumulator b complete
+      }
+      // Every MMA must have completed before TMEM is released.
+      mma_commit(drain);
+      drain_wait(drain, 0, args.err, args.limit_ns);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue ---
+    const int q = warp & 3;  // this warp's TMEM lane quarter
+    int lt = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&tfull[b], tph, wctl, kErrTimeoutEpilogue) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      int e, at, wt;
+      decode_tile(t, e, at, wt);
+      const int act_row0 = s_off[e] + at * C::ACT_ROWS;
+      const int act_end = s_off[e + 1];
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      if (!SWAP) {
+        const int row = act_row0 + q * 32 + lane;
+        const bool valid = row < act_end;
+        uint16_t* orow = args.out + (size_t)(valid ? row : 0) * args.out_ld;
+        if (GLU) {
+          const int col0 = wt * (BN / 2);
+#pragma unroll 1
+          for (int c = 0; c < BN / 2; c += 16) {
+            float a[16], g[16];
+            tmem_ld_2x16(tacc + c, tacc + BN / 2 + c, a, g);
+            if (valid) {
+              uint32_t p[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                p[i] = pack_bf16x2(silu_mul(a[2 * i], g[2 * i]), silu_mul(a[2 * i + 1], g[2 * i + 1]));
+              uint4* dst = reinterpret_cast<uint4*>(orow + col0 + c);
+              dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+              dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            }
+          }
+        } else {
+          const int col0 = wt * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float a[16], g[16];
+            tmem_ld_2x16(tacc + c, tacc + c + 16, a, g);
+            if (valid) {
+              uint32_t p[16];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                p[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+                p[8 + i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(orow + col0 + c);
+              dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+              dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+              dst[2] = make_uint4(p[8], p[9], p[10], p[11]);
+              dst[3] = make_uint4(p[12], p[13], p[14], p[15]);
+            }
+          }
+        }
+      } else {
+        // lane <-> weight row j (output column); TMEM columns <-> token rows
+        const int j = wt * 128 + q * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float a[16], g[16];
+          tmem_ld_2x16(tacc + c, tacc + (GLU ? BN : 0) + c, a, g);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int row = act_row0 + c + i;
+            if (row < act_end) {
+              const float v = GLU ? silu_mul(a[i], g[i]) : a[i];
+              const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+              args.out[(size_t)row * args.out_ld + j] = *reinterpret_cast<const uint16_t*>(&hv);
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl w{&abort_flag, err, limit_ns};
+    (void)mbar_wait(&bar, 0, w, kErrTimeoutSelftest);  // nothing ever arrives
+  }
+}
+
+// ------------------------------------------------------------------ host ---
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols], box of box_cols x box_rows, 128-byte swizzle.
+static bool encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                      uint32_t box_cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWAP, bool GLU, int BN, int STAGES>
+static cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
+                            const GemmArgs& args, int grid, cudaStream_t st) {
+  using C = GemmCfg<SWAP, GLU, BN, STAGES>;
+  auto kern = grouped_gemm_kernel<SWAP, GLU, BN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(a, w0, w1, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
+                              const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                              uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
+                              cudaStream_t st) {
+  const int R = s.T * s.top_k;
+  if (R == 0) return cudaSuccess;
+  const int d = s.dim, hd = s.hidden, n = s.n_experts;
+  const bool stream = path == MOE_FFN_WEIGHT_STREAM ||
+                      (path == MOE_FFN_AUTO && s.T <= kAutoStreamMaxT);
+  const int grid = num_sms();
+  CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
+  GemmArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd};
+  GemmArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, 0, d, d};
+  cudaError_t e;
+  if (!stream) {
+    if (!encode_2d(&tm_x, x_perm, d, R, 64, 128) ||
+        !encode_2d(&tm_w1, w1, d, (uint64_t)n * hd, 64, 128) ||
+        !encode_2d(&tm_w3, w3, d, (uint64_t)n * hd, 64, 128) ||
+        !encode_2d(&tm_h, h, hd, R, 64, 128))
+      return cudaErrorInvalidValue;
+    e = run_gemm<false, true, 256, 4>(tm_x, tm_w1, tm_w3, a1, grid, st);
+    if (e != cudaSuccess) return e;
+    if (d % 256 == 0) {
+      if (!encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 64, 256)) return cudaErrorInvalidValue;
+      a2.w_tiles = d / 256;
+      return run_gemm<false, false, 256, 4>(tm_h, tm_w2, tm_w2, a2, grid, st);
+    }
+    if (!encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 64, 128)) return cudaErrorInvalidValue;
+    a2.w_tiles = d / 128;
+    return run_gemm<false, false, 128, 6>(tm_h, tm_w2, tm_w2, a2, grid, st);
+  }
+  if (!encode_2d(&tm_x, x_perm, d, R, 64, kStreamTokens) ||
+      !encode_2d(&tm_w1, w1, d, (uint64_t)n * hd, 64, 128) ||
+      !encode_2d(&tm_w3, w3, d, (uint64_t)n * hd, 64, 128) ||
+      !encode_2d(&tm_h, h, hd, R, 64, kStreamTokens) ||
+      !encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 64, 128))
+    return cudaErrorInvalidValue;
+  e = run_gemm<true, true, kStreamTokens, 6>(tm_x, tm_w1, tm_w3, a1, grid, st);
+  if (e != cudaSuccess) return e;
+  a2.w_tiles = d / 128;
+  return run_gemm<true, false, kStreamTokens, 10>(tm_h, tm_w2, tm_w2, a2, grid, st);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,62 @@
+// internal.h -- host-side declarations shared by the .cu files of the library:
+// workspace layout and kernel launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 32;
+constexpr int kPermuteChunk = 256;       // assignments per permute block
+constexpr int kStreamTokens = 32;        // token chunk (MMA N) of the weight stream
+constexpr int kAutoStreamMaxT = 32;      // MOE_FFN_AUTO: weight stream when T <= this
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+// Device workspace layout: one header page, then 256-byte aligned arrays.
+struct WsLayout {
+  size_t err;          // uint32 error word (header)
+  size_t ids;          // int32 [R]
+  size_t gates;        // f32 [R]
+  size_t counts;       // int32 [n]
+  size_t offsets;      // int32 [n + 1]
+  size_t chunk_hist;   // int32 [nchunks * n]
+  size_t chunk_base;   // int32 [nchunks * n]
+  size_t perm_src;     // int32 [R]
+  size_t slot_row;     // int32 [R]
+  size_t u;            // bf16 [T, dim] (RMSNorm output)
+  size_t x_perm;       // bf16 [R, dim]
+  size_t h;            // bf16 [R, hidden]
+  size_t y_perm;       // bf16 [R, dim]
+  size_t total;
+  int nchunks;
+};
+
+bool shape_supported(const moe_shape* s);
+WsLayout ws_layout(const moe_shape* s);
+
+// Launchers: return cudaSuccess or the launch error.
+cudaError_t launch_router(const moe_shape& s, const uint16_t* x, const uint16_t* wg, int32_t* ids,
+                          float* gates, int32_t* counts, uint16_t* u_out, float eps,
+                          cudaStream_t st);
+cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
+                           int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
+                           int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
+                           uint16_t* x_perm, int nchunks, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* slot_row,
+                           const float* gates, const uint16_t* residual, uint16_t* y,
+                           cudaStream_t st);
+// Grouped expert FFN; returns cudaErrorInvalidValue when a tensor map cannot
+// be encoded.
+cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
+                              const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                              uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
+                              cudaStream_t st);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

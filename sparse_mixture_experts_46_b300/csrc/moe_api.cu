@@ -1,0 +1,242 @@
+// moe_api.cu -- the extern "C" entry points declared in include/moe.h:
+// argument and shape validation, the workspace layout, and the launch order of
+// the router, grouping, expert FFN and combine kernels on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+bool shape_supported(const moe_shape* s) {
+  if (s == nullptr) return false;
+  if (s->T < 0 || s->n_experts < 1 || s->n_experts > kMaxExperts) return false;
+  if (s->top_k < 1 || s->top_k > s->n_experts) return false;
+  if (s->dim < 128 || s->dim % 128 != 0) return false;
+  if (s->hidden < 128 || s->hidden % 128 != 0) return false;
+  const int64_t R = (int64_t)s->T * s->top_k;
+  const int64_t wide = s->dim > s->hidden ? s->dim : s->hidden;
+  if (R * wide >= (int64_t(1) << 31)) return false;
+  if ((int64_t)s->n_experts * s->hidden >= (int64_t(1) << 31)) return false;
+  if ((int64_t)s->n_experts * s->dim >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+static size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const moe_shape* s) {
+  WsLayout L{};
+  const size_t T = (size_t)s->T, R = T * (size_t)s->top_k, n = (size_t)s->n_experts;
+  L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
+  size_t off = 0;
+  L.err = off;
+  off += 4096;  // header page
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L.ids = take(R * 4);
+  L.gates = take(R * 4);
+  L.counts = take(n * 4);
+  L.offsets = take((n + 1) * 4);
+  L.chunk_hist = take((size_t)L.nchunks * n * 4);
+  L.chunk_base = take((size_t)L.nchunks * n * 4);
+  L.perm_src = take(R * 4);
+  L.slot_row = take(R * 4);
+  L.u = take(T * (size_t)s->dim * 2);
+  L.x_perm = take(R * (size_t)s->dim * 2);
+  L.h = take(R * (size_t)s->hidden * 2);
+  L.y_perm = take(R * (size_t)s->dim * 2);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+template <typename P>
+bool aligned16(P* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+template <typename P>
+bool ok_ptr(P* p) {
+  return p != nullptr && aligned16(p);
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+  if (!shape_supported(shape)) return 0;
+  return ws_layout(shape).total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_ptr(ws) || ws_bytes < 4096) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 4096, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_topk(const moe_shape* shape, const moe_bf16* x, const moe_bf16* w_gate,
+                           int32_t* ids, float* gates, int32_t* counts, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ok_ptr(counts)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(ids) || !ok_ptr(gates)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router(*shape, x, w_gate, ids, gates, counts, nullptr, 0.0f,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_permute(const moe_shape* shape, const moe_bf16* x, const int32_t* ids,
+                       int32_t* offsets, int32_t* perm_src, int32_t* slot_row, moe_bf16* x_perm,
+                       void* ws, size_t ws_bytes, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ok_ptr(offsets) || !ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(perm_src) || !ok_ptr(slot_row) ||
+                       !ok_ptr(x_perm)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(shape);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_permute(*shape, x, ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
+                                    at<int32_t>(ws, L.chunk_base), perm_src, slot_row, x_perm,
+                                    L.nchunks, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn_grouped(const moe_shape* shape, const moe_bf16* x_perm,
+                                  const int32_t* offsets, const moe_bf16* w1, const moe_bf16* w3,
+                                  const moe_bf16* w2, moe_bf16* h, moe_bf16* y_perm, int32_t path,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (path < MOE_FFN_AUTO || path > MOE_FFN_WEIGHT_STREAM) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(w1) || !ok_ptr(w3) ||
+                       !ok_ptr(w2) || !ok_ptr(h) || !ok_ptr(y_perm)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(shape);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const cudaError_t e = launch_expert_ffn(*shape, x_perm, offsets, w1, w3, w2, h, y_perm, path,
+                                          at<uint32_t>(ws, L.err),
+                                          static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+moe_status moe_combine(const moe_shape* shape, const moe_bf16* y_perm, const int32_t* slot_row,
+                       const float* gates, const moe_bf16* residual, moe_bf16* y, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (shape->T > 0 && (!ok_ptr(y_perm) || !ok_ptr(slot_row) || !ok_ptr(gates) || !ok_ptr(y)))
+    return MOE_ERR_INVALID_ARG;
+  if (residual != nullptr && !aligned16(residual)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*shape, y_perm, slot_row, gates, residual, y,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
+                             const moe_bf16* x, const moe_bf16* w_gate, const moe_bf16* w1,
+                             const moe_bf16* w3, const moe_bf16* w2, moe_bf16* y, int32_t* ids,
+                             float* gates, void* ws, size_t ws_bytes, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  const int path = opts ? opts->ffn_path : MOE_FFN_AUTO;
+  if (path < MOE_FFN_AUTO || path > MOE_FFN_WEIGHT_STREAM) return MOE_ERR_INVALID_ARG;
+  const bool norm = opts && opts->use_rmsnorm;
+  if (norm && !(opts->rmsnorm_eps > 0.0f)) return MOE_ERR_INVALID_ARG;
+  const moe_bf16* residual = opts ? opts->residual : nullptr;
+  if (residual != nullptr && !aligned16(residual)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(w1) || !ok_ptr(w3) ||
+                       !ok_ptr(w2) || !ok_ptr(y)))
+    return MOE_ERR_INVALID_ARG;
+  if ((ids != nullptr && !aligned16(ids)) || (gates != nullptr && !aligned16(gates)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(shape);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (shape->T == 0) return MOE_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* d_ids = ids ? ids : at<int32_t>(ws, L.ids);
+  float* d_gates = gates ? gates : at<float>(ws, L.gates);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  uint16_t* u = norm ? at<uint16_t>(ws, L.u) : nullptr;
+  const uint16_t* src = norm ? u : x;
+
+  cudaError_t e = launch_router(*shape, x, w_gate, d_ids, d_gates, counts, u,
+                                norm ? opts->rmsnorm_eps : 0.0f, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_permute(*shape, src, d_ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
+                     at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src),
+                     at<int32_t>(ws, L.slot_row), at<uint16_t>(ws, L.x_perm), L.nchunks, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_expert_ffn(*shape, at<uint16_t>(ws, L.x_perm), offsets, w1, w3, w2,
+                        at<uint16_t>(ws, L.h), at<uint16_t>(ws, L.y_perm), path,
+                        at<uint32_t>(ws, L.err), st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_combine(*shape, at<uint16_t>(ws, L.y_perm), at<int32_t>(ws, L.slot_row), d_gates,
+                     residual, y, st);
+  return cuda_status(e);
+}
+
+moe_status moe_check_error(void* ws, void* stream) {
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_ERR_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream) {
+  if (!ok_ptr(ws) || ws_bytes < 4096) return MOE_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_selftest(static_cast<uint32_t*>(ws), limit_ns,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

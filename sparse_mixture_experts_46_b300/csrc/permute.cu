@@ -1,0 +1,134 @@
+// permute.cu -- expert grouping of the T*K assignments (the per-expert token
+// groups of "Mixtral of Experts" section 2.1: experts receive different
+// numbers of tokens and each group is processed as one dense block).
+//
+// The grouped order is the stable sort of the flat assignments a = t*K + k by
+// expert id.  It is built without any order-dependent atomics, so it is
+// bit-reproducible:
+//   1. hist:    every block of kPermuteChunk assignments counts its experts;
+//   2. scan:    one block turns the [chunk, expert] counts into per-expert
+//               totals, offsets (exclusive prefix over experts) and each
+//               chunk's first row inside every expert group;
+//   3. scatter: every block ranks its assignments inside their expert
+//               (warp match + popcount, then a prefix over the block's warps),
+//               writing slot_row[a] and perm_src[row];
+//   4. gather:  x_perm[row] = x[perm_src[row]], one warp per row, 16-byte
+//               vector moves.
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(kPermuteChunk) permute_hist_kernel(const int32_t* __restrict__ ids,
+                                                                     int R, int n,
+                                                                     int32_t* __restrict__ hist) {
+  __shared__ int s[kMaxExperts];
+  if (threadIdx.x < kMaxExperts) s[threadIdx.x] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * kPermuteChunk + threadIdx.x;
+  if (a < R) {
+    const int e = ids[a];
+    if ((unsigned)e < (unsigned)n) atomicAdd(&s[e], 1);  // ids outside [0, n) are ignored
+  }
+  __syncthreads();
+  if (threadIdx.x < n) hist[(size_t)blockIdx.x * n + threadIdx.x] = s[threadIdx.x];
+}
+
+// One block of 32 threads: thread e owns expert e.
+__global__ void __launch_bounds__(32) permute_scan_kernel(const int32_t* __restrict__ hist,
+                                                          int nchunks, int n,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ chunk_base) {
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < n) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = hist[(size_t)c * n + e];
+      chunk_base[(size_t)c * n + e] = total;  // rank of the chunk's first row inside expert e
+      total += v;
+    }
+  }
+  // exclusive prefix over experts (lanes >= n contribute 0)
+  int incl = total;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (e >= o) incl += v;
+  }
+  const int excl = incl - total;
+  if (e < n) {
+    if (counts) counts[e] = total;
+    offsets[e] = excl;
+    for (int c = 0; c < nchunks; ++c) chunk_base[(size_t)c * n + e] += excl;
+  }
+  if (e == n - 1) offsets[n] = incl;
+}
+
+__global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
+    const int32_t* __restrict__ ids, int R, int K, int n, const int32_t* __restrict__ chunk_base,
+    int32_t* __restrict__ perm_src, int32_t* __restrict__ slot_row) {
+  constexpr int kWarps = kPermuteChunk / 32;
+  __shared__ int wcnt[kWarps][kMaxExperts];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+
+  const int a = blockIdx.x * kPermuteChunk + threadIdx.x;
+  int e = (a < R) ? ids[a] : -1;
+  if ((unsigned)e >= (unsigned)n) e = -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned lower = peers & ((1u << lane) - 1u);
+  const int rank_in_warp = __popc(lower);
+  if (e >= 0 && lower == 0) wcnt[warp][e] = __popc(peers);  // group leader
+  __syncthreads();
+  if (e >= 0) {
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wcnt[w][e];
+    const int row = chunk_base[(size_t)blockIdx.x * n + e] + before + rank_in_warp;
+    slot_row[a] = row;
+    perm_src[row] = a / K;
+  }
+}
+
+// x_perm[r, :] = x[perm_src[r], :]; one warp per row, 16 bytes per lane-step.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm_src,
+                                                          int R, int d, int T,
+                                                          uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int vec = d / 8;  // uint4 per row
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < R; r += gridDim.x * wpb) {
+    const int t = perm_src[r];
+    if ((unsigned)t >= (unsigned)T) continue;  // only reachable with ids outside [0, n)
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
+    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
+                           int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
+                           int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
+                           uint16_t* x_perm, int nchunks, cudaStream_t st) {
+  const int R = s.T * s.top_k;
+  if (nchunks > 0) {
+    permute_hist_kernel<<<nchunks, kPermuteChunk, 0, st>>>(ids, R, s.n_experts, chunk_hist);
+  }
+  permute_scan_kernel<<<1, 32, 0, st>>>(chunk_hist, nchunks, s.n_experts, counts_out, offsets,
+                                        chunk_base);
+  if (R == 0) return cudaGetLastError();
+  permute_scatter_kernel<<<nchunks, kPermuteChunk, 0, st>>>(ids, R, s.top_k, s.n_experts,
+                                                            chunk_base, perm_src, slot_row);
+  if (x_perm != nullptr) {
+    int blocks = (R + 7) / 8;
+    const int cap = num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    gather_rows_kernel<<<blocks, 256, 0, st>>>(x, perm_src, R, s.dim, s.T, x_perm);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

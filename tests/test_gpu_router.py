@@ -1,0 +1,75 @@
+"""GPU router (moe_router_topk) against the fp64 oracle: ids and counts
+bit-exact, gates within 1e-5, on gap-filtered inputs."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as orc
+from tests.gpu_util import dev_bf16, lib
+from tests.inputs_filtered import filter_x
+
+pytestmark = pytest.mark.gpu
+
+
+def run_router(cfg, x_bits, wg_bits):
+    moe = lib()
+    T, K, n = cfg.T, cfg.top_k, cfg.n_experts
+    ids = torch.full((max(T, 1), K), -7, dtype=torch.int32, device="cuda")
+    gates = torch.full((max(T, 1), K), -7.0, dtype=torch.float32, device="cuda")
+    counts = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    x = dev_bf16(x_bits) if T > 0 else torch.empty((1, cfg.dim), dtype=torch.bfloat16, device="cuda")
+    moe.moe_router_topk(cfg, x, dev_bf16(wg_bits), ids, gates, counts)
+    torch.cuda.synchronize()
+    return ids[:T].cpu().numpy(), gates[:T].cpu().numpy(), counts.cpu().numpy()
+
+
+def check_router(cfg, x_bits, wg_bits):
+    ids, gates, counts = run_router(cfg, x_bits, wg_bits)
+    r_ids, r_gates, _ = orc.router(x_bits, wg_bits, cfg.top_k)
+    assert np.array_equal(ids, r_ids), np.argwhere(ids != r_ids)[:5]
+    assert np.max(np.abs(gates - r_gates), initial=0.0) < 1e-5
+    assert np.array_equal(counts, np.bincount(r_ids.reshape(-1), minlength=cfg.n_experts))
+
+
+def layer_inputs(cfg):
+    x = mi.gen_x(cfg)
+    wg = mi.gen_router_weight(cfg)
+    filter_x(cfg, x, wg)
+    return x, wg
+
+
+@pytest.mark.parametrize("T,dim,n,K", [
+    (64, 128, 8, 2), (1, 128, 8, 2), (2, 256, 8, 2), (127, 128, 8, 2), (129, 384, 8, 2),
+    (300, 128, 1, 1), (200, 128, 8, 8), (200, 128, 5, 3), (150, 256, 16, 2), (100, 128, 32, 4),
+    (77, 128, 12, 1)])
+def test_router_matches_oracle(T, dim, n, K):
+    cfg = mi.Config("r", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=700 + T + n)
+    x, wg = layer_inputs(cfg)
+    check_router(cfg, x, wg)
+
+
+def test_router_exact_ties_go_to_lower_index():
+    cfg = mi.Config("tie", T=33, dim=128, hidden=128)
+    x = np.zeros((33, 128), np.uint16)      # all logits exactly 0
+    wg = mi.gen_router_weight(cfg)
+    ids, gates, counts = run_router(cfg, x, wg)
+    assert np.all(ids == np.array([0, 1]))
+    assert np.all(gates == 0.5)
+    assert counts.tolist() == [33, 33, 0, 0, 0, 0, 0, 0]
+
+
+def test_router_zero_tokens_clears_counts():
+    cfg = mi.Config("empty", T=0, dim=128, hidden=128)
+    _, _, counts = run_router(cfg, np.zeros((0, 128), np.uint16), mi.gen_router_weight(cfg))
+    assert np.all(counts == 0)
+
+
+@pytest.mark.parametrize("name", ["prefill", "skew"])
+def test_router_full_size(name):
+    cfg = mi.CONFIGS[name]
+    wg = mi.gen_router_weight(cfg)
+    shift = mi.skew_shift(cfg, wg) if cfg.zipf_s > 0 else None
+    x = mi.gen_x(cfg, 0, shift)
+    filter_x(cfg, x, wg, shift)
+    check_router(cfg, x, wg)
