@@ -1,6 +1,7 @@
 """Build the CUDA library libmoe_b300.so in-tree with nvcc for sm_103a.
 
-Usage: ``python -m sparse_mixture_experts_46_b300.build [--verbose]``.
+Usage: ``python sparse_mixture_experts_46_b300/build.py [--force] [--verbose]`` (run
+it as a file: importing the package would load the library it is rebuilding).
 The library is rebuilt when any source under csrc/ or include/ is newer.
 """
 from __future__ import annotations

@@ -14,10 +14,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "moe.h")
 
 
+def build_module():
+    import __graft_entry__
+    return __graft_entry__._build_module()
+
+
 @pytest.fixture(scope="module")
 def lib():
-    from sparse_mixture_experts_46_b300 import build
-    path = build.build()
+    path = build_module().build()
     return ctypes.CDLL(path)
 
 
@@ -43,8 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_built_for_sm103a_only():
-    from sparse_mixture_experts_46_b300 import build
-    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert build_module().ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 class Shape(ctypes.Structure):
