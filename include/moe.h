@@ -164,6 +164,30 @@ MOE_API moe_status moe_check_error(void* ws, void* stream);
 MOE_API moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes,
                                      uint64_t limit_ns, void* stream);
 
+/* moe_permute without a workspace (the paper has no counterpart: this is an
+ * interface convenience, not a step of the method).  Same outputs, same
+ * kernels and same argument rules as moe_permute, but the call takes no `ws`
+ * and allocates nothing: its scratch (two [chunk][expert] count tables) lives
+ * in a fixed 512 KiB device array inside this library, held on every GPU that
+ * loads the library until the process exits.
+ *
+ * It is meant for callers that receive only their input and output buffers
+ * from a host framework (a plugin or custom-operator interface without a
+ * workspace argument) and may not call cudaMalloc themselves, because the
+ * framework owns all device memory or forbids allocation during a step.
+ *
+ * Limit: ceil(T*K / 256) * n_experts <= 65536 (T*K <= 2,097,152 for n = 8);
+ * larger shapes return MOE_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * All calls share the one array: calls that may overlap on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller.
+ * Each call overwrites the tables completely before reading them. */
+MOE_API moe_status moe_permute_noalloc(const moe_shape* shape, const moe_bf16* x,
+                                       const int32_t* ids, int32_t* offsets,
+                                       int32_t* perm_src, int32_t* slot_row,
+                                       moe_bf16* x_perm, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ MOE_FFN_WEIGHT_STREAM = 2
 EXPORTS = (
     "moe_status_string", "moe_workspace_bytes", "moe_workspace_init", "moe_router_topk",
     "moe_permute", "moe_expert_ffn_grouped", "moe_combine", "moe_layer_forward",
-    "moe_check_error", "moe_selftest_wait_timeout",
+    "moe_check_error", "moe_selftest_wait_timeout", "moe_permute_noalloc",
 )
 
 
@@ -71,6 +71,7 @@ def _load() -> ctypes.CDLL:
                                     vp, vp, sz, vp]),
         "moe_check_error": (i32, [vp, vp]),
         "moe_selftest_wait_timeout": (i32, [vp, sz, ctypes.c_uint64, vp]),
+        "moe_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,3 +215,15 @@ def moe_selftest_wait_timeout(ws, limit_ns: int, stream=None) -> None:
     _check(_LIB.moe_selftest_wait_timeout(_ptr(ws, name="ws"), ws.numel() * ws.element_size(),
                                           int(limit_ns), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_permute_noalloc(shape, x, ids, offsets, perm_src, slot_row, x_perm, stream=None) -> None:
+    """moe_permute for callers that cannot allocate a workspace: the library's
+    own fixed device scratch is used instead (see include/moe.h)."""
+    s = _shape(shape)
+    _check(_LIB.moe_permute_noalloc(ctypes.byref(s), _ptr(x, _BF16, "x"), _ptr(ids, _I32, "ids"),
+                                    _ptr(offsets, _I32, "offsets"),
+                                    _ptr(perm_src, _I32, "perm_src"),
+                                    _ptr(slot_row, _I32, "slot_row"),
+                                    _ptr(x_perm, _BF16, "x_perm"), _stream(stream)),
+           "moe_permute_noalloc")

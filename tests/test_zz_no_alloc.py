@@ -1,0 +1,59 @@
+"""moe_permute_noalloc: the expert grouping for callers that cannot allocate
+device memory (they are handed only input and output buffers by a host
+framework with no workspace argument, and may not call cudaMalloc themselves).
+It uses the library's fixed device scratch array instead of a caller
+workspace; its outputs must equal those of moe_permute, call after call."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from tests.gpu_util import dev_bf16, dev_i32, host_bits, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _outputs(cfg):
+    R = cfg.T * cfg.top_k
+    i32 = dict(dtype=torch.int32, device="cuda")
+    return (torch.full((cfg.n_experts + 1,), -3, **i32), torch.full((R,), -3, **i32),
+            torch.full((R,), -3, **i32),
+            torch.zeros((R, cfg.dim), dtype=torch.bfloat16, device="cuda"))
+
+
+def _host(outs):
+    off, src, slot, xp = outs
+    return off.cpu().numpy(), src.cpu().numpy(), slot.cpu().numpy(), host_bits(xp)
+
+
+def _case(T, n, K, dim, seed):
+    cfg = mi.Config("noalloc", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=seed)
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.permutation(n)[:K] for _ in range(T)]).astype(np.int32)
+    return cfg, dev_bf16(mi.gen_x(cfg)), dev_i32(ids)
+
+
+def test_noalloc_grouping_equals_workspace_grouping_twice():
+    moe = lib()
+    # two calls in a row with different shapes: the shared scratch keeps the
+    # first call's contents, which the second call must not depend on
+    for T, n, K, dim, seed in [(3000, 8, 2, 256, 11), (129, 5, 3, 128, 12)]:
+        cfg, x, ids = _case(T, n, K, dim, seed)
+        ref = _outputs(cfg)
+        moe.moe_permute(cfg, x, ids, *ref, moe.new_workspace(cfg))
+        got = _outputs(cfg)
+        moe.moe_permute_noalloc(cfg, x, ids, *got)
+        torch.cuda.synchronize()
+        for a, b in zip(_host(got), _host(ref)):
+            assert np.array_equal(a, b)
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    moe = lib()
+    cfg = mi.Config("big", T=2_200_000, dim=128, hidden=128, n_experts=8, top_k=1)
+    small = _outputs(mi.Config("s", T=1, dim=128, hidden=128, top_k=1))
+    x = torch.zeros((1, 128), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_permute_noalloc(cfg, x, ids, *small)
+    assert e.value.status == moe.MOE_ERR_WORKSPACE_TOO_SMALL
