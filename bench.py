@@ -38,10 +38,12 @@ DECODE, PREFILL = "decode", "prefill"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", choices=[DECODE, PREFILL], default=None,
+                   help="no timing: run W warm-up + K layer calls of one workload (for ncu)")
     return p.parse_args()
 
 
@@ -160,15 +162,16 @@ KERNELS_PER_LAYER = 8  # router, hist, scan, scatter, gather, gate/up GEMM, down
 # --------------------------------------------------------------- clocks ---
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples; only those inside the timed window count."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self):
         import torch
         self.proc = None
+        self.window = None
         try:
             uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
             ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -178,6 +181,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, AttributeError):
             self.proc = None
+        time.sleep(0.5)  # let nvidia-smi start sampling before the timed region
+
+    def mark(self, t0, t1):
+        """Wall-clock bounds (datetime) of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -188,24 +196,36 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows = []
         for line in out.splitlines():
             f = [v.strip() for v in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(f[1]), float(f[2]), float(f[3]), f[5:9]))
             except ValueError:
                 continue
-            for nm, v in zip(names, f[4:8]):
+        if self.window is not None:
+            lo = self.window[0] - datetime.timedelta(seconds=0.05)
+            hi = self.window[1] + datetime.timedelta(seconds=0.05)
+            inside = [r for r in rows if lo <= r[0] <= hi]
+        else:
+            inside = rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample inside the timed window (%d outside)" % len(rows)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names, r[4]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "power_w_median": statistics.median(r[3] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
 # --------------------------------------------------------------- traffic ---
@@ -289,6 +309,22 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def run_profile_case(args):
+    """One workload only, W + K layer calls through moe_layer_forward, no timing:
+    the small, single-layer case that ncu captures use."""
+    import torch
+    import sparse_mixture_experts_46_b300 as moe
+    cfg, L = load_layer(args.profile)
+    b = Buffers(cfg, L)
+    for _ in range(args.warmup + args.steps):
+        moe.moe_layer_forward(cfg, b.x, b.wg, b.w1, b.w3, b.w2, b.y, b.ws)
+    torch.cuda.synchronize()
+    st = moe.moe_check_error(b.ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: %d" % st)
+    print("profile case %s: %d layer calls ok" % (args.profile, args.warmup + args.steps))
+
+
 def config_block(layers):
     dc = layers[DECODE][0]
     return {"workload": "Mixtral-shaped MoE layer, decode batch T=16 + prefill batch T=4096 "
@@ -311,6 +347,9 @@ def main():
 
     import torch
     import sparse_mixture_experts_46_b300 as moe
+    if args.profile is not None:
+        run_profile_case(args)
+        return
     layers = {DECODE: load_layer(DECODE), PREFILL: load_layer(PREFILL)}
     bufs = {k: Buffers(cfg, L) for k, (cfg, L) in layers.items()}
     stream = torch.cuda.current_stream()
@@ -344,12 +383,16 @@ def main():
     clocks = ClockSampler()
     barrier(world)
     torch.cuda.synchronize()
+    import datetime
+    w0 = datetime.datetime.now()
     start.record(stream)
     for k in range(args.steps):
         step(evs[k])
     end.record(stream)
     torch.cuda.synchronize()
+    w1 = datetime.datetime.now()
     barrier(world)
+    clocks.mark(w0, w1)
     clk = clocks.stop()
     ms_total = max_over_ranks(start.elapsed_time(end), world)
     ms_step = ms_total / args.steps

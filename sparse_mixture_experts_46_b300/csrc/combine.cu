@@ -2,9 +2,9 @@
 // output is the gate-weighted sum of the selected experts' outputs).
 //
 // y[t] = bf16( sum_{k<K} gates[t,k] * y_perm[slot_row[t*K+k]]  (+ residual[t]) )
-// One warp per token, 16-byte vector loads of the K expert rows, fp32
-// accumulation in slot order k = 0..K-1 (a fixed order, so the result does not
-// depend on scheduling), residual added last.
+// 16-byte vector loads of the K expert rows, fp32 accumulation in slot order
+// k = 0..K-1 (a fixed order, so the result does not depend on scheduling),
+// residual added last.
 #include "device.cuh"
 #include "internal.h"
 
@@ -19,42 +19,45 @@ __device__ __forceinline__ void unpack8c(const uint4& v, float* f) {
   }
 }
 
+// One thread per 16-byte slice of an output row: thread i of the flat grid
+// writes slice i % (dim/8) of token i / (dim/8); every load it issues is
+// independent, so the whole output is in flight at once.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_row,
                                                       const float* __restrict__ gates,
                                                       const uint16_t* __restrict__ residual,
                                                       int T, int K, int d, int R,
                                                       uint16_t* __restrict__ y) {
-  const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  const int vec = d / 8;
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
-    for (int i = lane; i < vec; i += 32) {
-      float acc[8];
+  const int vec = d >> 3;
+  const int64_t total = (int64_t)T * vec;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / vec);
+    const int v = (int)(i - (int64_t)t * vec);
+    float acc[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-      for (int k = 0; k < K; ++k) {
-        const int row = slot_row[(size_t)t * K + k];
-        if ((unsigned)row >= (unsigned)R) continue;
-        const float g = gates[(size_t)t * K + k];
-        float v[8];
-        unpack8c(__ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row * d) + i), v);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const int row = __ldg(slot_row + (size_t)t * K + k);
+      if ((unsigned)row >= (unsigned)R) continue;
+      const float g = __ldg(gates + (size_t)t * K + k);
+      float f[8];
+      unpack8c(__ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row * d) + v), f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(g, v[j], acc[j]);
-      }
-      if (residual != nullptr) {
-        float r[8];
-        unpack8c(__ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * d) + i), r);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += r[j];
-      }
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(y + (size_t)t * d)[i] = o;
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(g, f[j], acc[j]);
     }
+    if (residual != nullptr) {
+      float r[8];
+      unpack8c(__ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * d) + v), r);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += r[j];
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(y + (size_t)t * d)[v] = o;
   }
 }
 
@@ -62,11 +65,12 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
                            const float* gates, const uint16_t* residual, uint16_t* y,
                            cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  int blocks = (s.T + 7) / 8;
-  const int cap = num_sms() * 8;
+  const int64_t total = (int64_t)s.T * (s.dim / 8);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<blocks, 256, 0, st>>>(y_perm, slot_row, gates, residual, s.T, s.top_k, s.dim,
-                                         s.T * s.top_k, y);
+  combine_kernel<<<(int)blocks, 256, 0, st>>>(y_perm, slot_row, gates, residual, s.T, s.top_k,
+                                              s.dim, s.T * s.top_k, y);
   return cudaGetLastError();
 }
 

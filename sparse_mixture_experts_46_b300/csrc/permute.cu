@@ -12,8 +12,8 @@
 //   3. scatter: every block ranks its assignments inside their expert
 //               (warp match + popcount, then a prefix over the block's warps),
 //               writing slot_row[a] and perm_src[row];
-//   4. gather:  x_perm[row] = x[perm_src[row]], one warp per row, 16-byte
-//               vector moves.
+//   4. gather:  x_perm[row] = x[perm_src[row]], 16-byte vector moves, one
+//               thread per slice.
 #include "device.cuh"
 #include "internal.h"
 
@@ -92,20 +92,22 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
   }
 }
 
-// x_perm[r, :] = x[perm_src[r], :]; one warp per row, 16 bytes per lane-step.
+// x_perm[r, :] = x[perm_src[r], :]; one thread per 16-byte slice of a row
+// (flat grid), so every row move is in flight at once.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm_src,
                                                           int R, int d, int T,
                                                           uint16_t* __restrict__ x_perm) {
-  const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  const int vec = d / 8;  // uint4 per row
-  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < R; r += gridDim.x * wpb) {
-    const int t = perm_src[r];
+  const int vec = d >> 3;
+  const int64_t total = (int64_t)R * vec;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vec);
+    const int v = (int)(i - (int64_t)r * vec);
+    const int t = __ldg(perm_src + r);
     if ((unsigned)t >= (unsigned)T) continue;  // only reachable with ids outside [0, n)
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
-    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+    reinterpret_cast<uint4*>(x_perm + (size_t)r * d)[v] =
+        __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v);
   }
 }
 
@@ -123,10 +125,11 @@ cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t*
   permute_scatter_kernel<<<nchunks, kPermuteChunk, 0, st>>>(ids, R, s.top_k, s.n_experts,
                                                             chunk_base, perm_src, slot_row);
   if (x_perm != nullptr) {
-    int blocks = (R + 7) / 8;
-    const int cap = num_sms() * 8;
+    const int64_t total = (int64_t)R * (s.dim / 8);
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    gather_rows_kernel<<<blocks, 256, 0, st>>>(x, perm_src, R, s.dim, s.T, x_perm);
+    gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(x, perm_src, R, s.dim, s.T, x_perm);
   }
   return cudaGetLastError();
 }

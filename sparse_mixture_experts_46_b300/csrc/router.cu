@@ -1,16 +1,18 @@
 // router.cu -- router logits, top-K selection and gate softmax
 // ("Mixtral of Experts" section 2.1, G(x) = Softmax(TopK(x . W_g))).
 //
-// One warp owns TPW tokens at a time.  Each lane walks the feature dimension
-// in 8-element (16-byte) slices, so a warp reads 512 contiguous bytes of every
-// token row per step; W_g rows are read through L1 and shared by the TPW
-// tokens.  Logits accumulate in fp32 (bf16 x bf16 products are exact in fp32)
-// and are reduced across the warp with butterfly shuffles, after which every
-// lane holds all n logits of its tokens.  Lane 0 then selects the top K
-// (strictly greater wins, scanning experts in ascending order, so ties go to
-// the lower index), computes the softmax of the selected logits and writes
-// ids / gates.  Per-expert counts are gathered in a shared histogram and
-// added to global memory once per block (integer atomics: order-free).
+// One 256-thread block owns TPB consecutive tokens.  The feature dimension is
+// split across all threads of the block in 8-element (16-byte) slices, so a
+// token row is read by the whole block at once and every thread issues its
+// loads independently (no long per-thread dependency chain); the W_g rows a
+// thread touches are loaded once and shared by the TPB tokens.  Products of
+// bf16 values are exact in fp32 and accumulate in fp32.  Partial logits are
+// reduced with warp butterflies, then across the 8 warps in a fixed order
+// (deterministic).  Thread tt < TPB then selects the top K of token tt:
+// strictly-greater wins while scanning experts in ascending order, so ties go
+// to the lower index; gates are the softmax of the selected logits.
+// Per-expert counts are gathered in a shared histogram and added to global
+// memory once per block (integer atomics: order-free).
 //
 // Optional RMSNorm (residual-stack workload): u = bf16(x / sqrt(mean(x^2)+eps))
 // is written out and the logits are taken on u, exactly as the expert FFN
@@ -19,6 +21,11 @@
 #include "internal.h"
 
 namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
@@ -37,160 +44,167 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int NE, int TPW>
-__global__ void __launch_bounds__(256) router_topk_kernel(
+}  // namespace
+
+template <int NE, int TPB>
+__global__ void __launch_bounds__(kThreads) router_topk_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, int T, int d, int n, int K,
     int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts,
     uint16_t* __restrict__ u_out, float eps) {
+  __shared__ float s_part[kWarps][TPB * NE];
+  __shared__ float s_logit[TPB * NE];
+  __shared__ float s_rs[TPB];
   __shared__ int s_hist[kMaxExperts];
-  if (threadIdx.x < kMaxExperts) s_hist[threadIdx.x] = 0;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int t0 = blockIdx.x * TPB;
+  const int nvec = d >> 3;  // 16-byte slices per row
+  const bool norm = (u_out != nullptr);
+  if (tid < kMaxExperts) s_hist[tid] = 0;
+
+  // ---- RMSNorm scale per token (sum of squares over the whole block)
+  if (norm) {
+    float ss[TPB];
+#pragma unroll
+    for (int tt = 0; tt < TPB; ++tt) ss[tt] = 0.0f;
+#pragma unroll 2
+    for (int v = tid; v < nvec; v += kThreads) {
+#pragma unroll
+      for (int tt = 0; tt < TPB; ++tt) {
+        if (t0 + tt < T) {
+          float f[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d) + v), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss[tt] = fmaf(f[i], f[i], ss[tt]);
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < TPB; ++tt) {
+      const float w = warp_sum(ss[tt]);
+      if (lane == 0) s_part[warp][tt] = w;
+    }
+    __syncthreads();
+    if (tid < TPB) {
+      float s = 0.0f;
+      for (int w = 0; w < kWarps; ++w) s += s_part[w][tid];
+      s_rs[tid] = 1.0f / sqrtf(s / (float)d + eps);
+    }
+    __syncthreads();
+  }
+
+  // ---- partial logits over this thread's slices
+  float acc[TPB][NE];
+#pragma unroll
+  for (int tt = 0; tt < TPB; ++tt)
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[tt][e] = 0.0f;
+
+#pragma unroll 2
+  for (int v = tid; v < nvec; v += kThreads) {
+    const int j0 = v * 8;
+    float xv[TPB][8];
+#pragma unroll
+    for (int tt = 0; tt < TPB; ++tt) {
+      if (t0 + tt < T) {
+        const size_t off = (size_t)(t0 + tt) * d + j0;
+        unpack8(__ldg(reinterpret_cast<const uint4*>(x + off)), xv[tt]);
+        if (norm) {
+          const float rs = s_rs[tt];
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            pk[i] = pack_bf16x2(xv[tt][2 * i] * rs, xv[tt][2 * i + 1] * rs);
+            xv[tt][2 * i] = __uint_as_float(pk[i] << 16);
+            xv[tt][2 * i + 1] = __uint_as_float(pk[i] & 0xFFFF0000u);
+          }
+          *reinterpret_cast<uint4*>(u_out + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv[tt][i] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      float w[NE];
+      const uint16_t* row = wg + (size_t)(j0 + jj) * n;
+      if (n == NE) {
+#pragma unroll
+        for (int q = 0; q < NE / 8; ++q) {
+          float f[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(row) + q), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[q * 8 + i] = f[i];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) w[e] = (e < n) ? bf16_bits_to_f32(__ldg(row + e)) : 0.0f;
+      }
+#pragma unroll
+      for (int tt = 0; tt < TPB; ++tt)
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[tt][e] = fmaf(xv[tt][jj], w[e], acc[tt][e]);
+    }
+  }
+
+  // ---- block reduction in a fixed order: warp butterflies, then warps 0..7
+#pragma unroll
+  for (int tt = 0; tt < TPB; ++tt)
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      const float s = warp_sum(acc[tt][e]);
+      if (lane == 0) s_part[warp][tt * NE + e] = s;
+    }
+  __syncthreads();
+  if (tid < TPB * NE) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += s_part[w][tid];
+    s_logit[tid] = s;
+  }
   __syncthreads();
 
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  const bool norm = (u_out != nullptr);
-
-  for (int t0 = (blockIdx.x * (blockDim.x >> 5) + warp) * TPW; t0 < T; t0 += warps_total * TPW) {
-    float rs[TPW];
-#pragma unroll
-    for (int tt = 0; tt < TPW; ++tt) rs[tt] = 1.0f;
-    if (norm) {
-      float ss[TPW];
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) ss[tt] = 0.0f;
-      for (int j0 = lane * 8; j0 < d; j0 += 256) {
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          if (t0 + tt < T) {
-            float v[8];
-            unpack8(*reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + j0), v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ss[tt] = fmaf(v[i], v[i], ss[tt]);
-          }
+  // ---- selection and gates: thread tt owns token t0 + tt
+  if (tid < TPB && t0 + tid < T) {
+    const int t = t0 + tid;
+    const float* l = s_logit + tid * NE;
+    uint32_t taken = 0;
+    float v0 = 0.0f, denom = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float best = 0.0f;
+      int bi = -1;
+      for (int e = 0; e < n; ++e) {
+        if (!((taken >> e) & 1u) && (bi < 0 || l[e] > best)) {
+          best = l[e];
+          bi = e;
         }
       }
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) {
-        ss[tt] = warp_sum(ss[tt]);
-        rs[tt] = 1.0f / sqrtf(ss[tt] / (float)d + eps);
-      }
+      taken |= 1u << bi;
+      if (k == 0) v0 = best;
+      denom += expf(best - v0);
+      ids[(size_t)t * K + k] = bi;
+      atomicAdd(&s_hist[bi], 1);
     }
-
-    float acc[TPW][NE];
-#pragma unroll
-    for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-      for (int e = 0; e < NE; ++e) acc[tt][e] = 0.0f;
-
-    for (int j0 = lane * 8; j0 < d; j0 += 256) {
-      float xv[TPW][8];
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) {
-        if (t0 + tt < T) {
-          const size_t off = (size_t)(t0 + tt) * d + j0;
-          unpack8(*reinterpret_cast<const uint4*>(x + off), xv[tt]);
-          if (norm) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              pk[i] = pack_bf16x2(xv[tt][2 * i] * rs[tt], xv[tt][2 * i + 1] * rs[tt]);
-              xv[tt][2 * i] = __uint_as_float(pk[i] << 16);
-              xv[tt][2 * i + 1] = __uint_as_float(pk[i] & 0xFFFF0000u);
-            }
-            *reinterpret_cast<uint4*>(u_out + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) xv[tt][i] = 0.0f;
-        }
-      }
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float w[NE];
-        const uint16_t* row = wg + (size_t)(j0 + jj) * n;
-        if (n == NE) {
-#pragma unroll
-          for (int q = 0; q < NE / 8; ++q) {
-            float f[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(row) + q), f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[q * 8 + i] = f[i];
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < NE; ++e) w[e] = (e < n) ? bf16_bits_to_f32(__ldg(row + e)) : 0.0f;
-        }
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-          for (int e = 0; e < NE; ++e) acc[tt][e] = fmaf(xv[tt][jj], w[e], acc[tt][e]);
-      }
-    }
-
-#pragma unroll
-    for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-      for (int e = 0; e < NE; ++e) acc[tt][e] = warp_sum(acc[tt][e]);
-
-    if (lane == 0) {
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) {
-        const int t = t0 + tt;
-        if (t >= T) break;
-        uint32_t taken = 0;
-        float v0 = 0.0f, denom = 0.0f;
-        // pass 1: select in order, accumulate the softmax denominator
-        for (int k = 0; k < K; ++k) {
-          float best = 0.0f;
-          int bi = -1;
-#pragma unroll
-          for (int e = 0; e < NE; ++e) {
-            if (e < n && !((taken >> e) & 1u) && (bi < 0 || acc[tt][e] > best)) {
-              best = acc[tt][e];
-              bi = e;
-            }
-          }
-          taken |= 1u << bi;
-          if (k == 0) v0 = best;
-          denom += expf(best - v0);
-          ids[(size_t)t * K + k] = bi;
-          atomicAdd(&s_hist[bi], 1);
-        }
-        // pass 2: the same selection again, now writing normalised gates
-        taken = 0;
-        const float inv = 1.0f / denom;
-        for (int k = 0; k < K; ++k) {
-          float best = 0.0f;
-          int bi = -1;
-#pragma unroll
-          for (int e = 0; e < NE; ++e) {
-            if (e < n && !((taken >> e) & 1u) && (bi < 0 || acc[tt][e] > best)) {
-              best = acc[tt][e];
-              bi = e;
-            }
-          }
-          taken |= 1u << bi;
-          gates[(size_t)t * K + k] = expf(best - v0) * inv;
-        }
-      }
+    const float inv = 1.0f / denom;
+    for (int k = 0; k < K; ++k) {
+      const int e = ids[(size_t)t * K + k];
+      gates[(size_t)t * K + k] = expf(l[e] - v0) * inv;
     }
   }
   __syncthreads();
-  if (threadIdx.x < n && s_hist[threadIdx.x] != 0) atomicAdd(&counts[threadIdx.x], s_hist[threadIdx.x]);
+  if (tid < n && s_hist[tid] != 0) atomicAdd(&counts[tid], s_hist[tid]);
 }
 
-template <int NE, int TPW>
+template <int NE, int TPB>
 static cudaError_t launch_router_t(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
                                    int32_t* ids, float* gates, int32_t* counts, uint16_t* u_out,
                                    float eps, cudaStream_t st) {
-  const int warps_needed = (s.T + TPW - 1) / TPW;
-  int blocks = (warps_needed + 7) / 8;
-  const int cap = num_sms() * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  router_topk_kernel<NE, TPW><<<blocks, 256, 0, st>>>(x, wg, s.T, s.dim, s.n_experts, s.top_k,
-                                                      ids, gates, counts, u_out, eps);
+  const int blocks = (s.T + TPB - 1) / TPB;
+  router_topk_kernel<NE, TPB><<<blocks, kThreads, 0, st>>>(x, wg, s.T, s.dim, s.n_experts,
+                                                           s.top_k, ids, gates, counts, u_out, eps);
   return cudaGetLastError();
 }
 
