@@ -67,14 +67,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """Largest value over all ranks (the slowest replica sets the step time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_per_step_max):
+    """Whole-job throughput: every replica processes its own batch (weak scaling)."""
+    return world * tokens_per_rank / (ms_per_step_max * 1e-3)
 
 
 # ------------------------------------------------------------- workload ---
@@ -230,19 +236,32 @@ class ClockSampler:
 
 # --------------------------------------------------------------- traffic ---
 
+GEMM_SOURCES = ("grouped_gemm.cu", "device.cuh")
+
+
+def gemm_source_digest():
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "sparse_mixture_experts_46_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic():
-    """Per-launch DRAM traffic of the dominant unit from the committed ncu summary,
-    or None when the kernel source changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "sparse_mixture_experts_46_b300", "csrc", "grouped_gemm.cu")
+    """Per-launch DRAM traffic of the dominant unit from the committed ncu summary
+    (profiles/traffic.txt), or None when the kernel sources changed since it was captured."""
     try:
-        rec = json.load(open(path))
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        rec = dict(line.strip().split("=", 1) for line in open(
+            os.path.join(ROOT, "profiles", "traffic.txt")) if "=" in line and
+            not line.startswith("#"))
     except (OSError, ValueError):
         return None
-    if rec.get("grouped_gemm_sha") != digest:
+    if rec.get("grouped_gemm_sha") != gemm_source_digest():
         return None
-    return rec.get("prefill_ffn_bytes_per_launch")
+    try:
+        return int(rec["prefill_ffn_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def peaks():
@@ -450,20 +469,26 @@ def main():
     tokens = sum(layers[n][0].T for n in (DECODE, PREFILL))
     io_bytes = sum(2 * layers[n][0].T * layers[n][0].dim for n in (DECODE, PREFILL))
     result = {
-        "metric": METRIC, "value": world * tokens / (ms_step * 1e-3), "unit": "tokens/s",
+        "metric": METRIC, "value": job_tokens_per_s(tokens, world, ms_step), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator, Table 1 shapes, random-init weights)",
         "config": config_block(layers),
+        # the kernel is timed inside a ~1 s back-to-back loop (power cap reached):
+        # its denominator is the sustained measured peak; the burst fraction is kept beside it
         "roofline": {"bound": "tensor", "achieved": pre["ffn_tflops"],
-                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": pre["ffn_tflops"] / pk["bf16_tflops"],
-                     "traffic": recorded_traffic(), "peak_kind": pk_kind,
-                     "frac_of_sustained": pre["ffn_tflops"] / pk["bf16_tflops_sustained"],
-                     "kernel": "prefill expert FFN: gate/up + down tcgen05 grouped GEMMs, "
-                               "6*T*K*dim*hidden FLOP per launch"},
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": pre["ffn_tflops"] / pk["bf16_tflops_sustained"],
+                     "traffic": recorded_traffic(),
+                     "peak_kind": pk_kind + " sustained bf16 (cuBLAS, 4 s loop)",
+                     "frac_of_burst": pre["ffn_tflops"] / pk["bf16_tflops"],
+                     "algorithmic_flop_per_launch": 6.0 * bufs[PREFILL].cfg.T
+                     * bufs[PREFILL].cfg.top_k * bufs[PREFILL].cfg.dim
+                     * bufs[PREFILL].cfg.hidden,
+                     "kernel": "prefill expert FFN: gate/up + down tcgen05 grouped GEMMs "
+                               "(one moe_expert_ffn_grouped call)"},
         "layers": per,
-        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                 "ms_per_step": e2e_ms},
         "gpu_launches": KERNELS_PER_LAYER * 2 * args.steps,

@@ -282,3 +282,17 @@ def test_random_routing_matches_printed_expectations():
     assert round(exp_either * 100) == g["first_or_second_repeat_printed_percent"]
     assert abs(first - g["first_choice_repeat"]) < 0.015
     assert abs(either - exp_either) < 0.025
+
+
+def test_stack_layer_residual_and_zero_experts():
+    """x + MoE(RMSNorm(x)): with W2 = 0 every expert outputs 0, so the block is the
+    identity; with identical experts it is x + FFN(RMSNorm(x))."""
+    rng = np.random.default_rng(60)
+    x, wg, w1, w3, w2 = _rand_layer(rng, 12, 16, 8, 4)
+    xb = orc.round_bf16(x)
+    out, _, _, _ = orc.stack_layer(xb, wg, w1, w3, np.zeros_like(w2), 2, 1e-5)
+    assert np.array_equal(out, orc.widen_bf16(xb))
+    W1, W3, W2 = (np.repeat(w[:1], 4, 0) for w in (w1, w3, w2))
+    out, _, _, u = orc.stack_layer(xb, wg, W1, W3, W2, 2, 1e-5)
+    want = orc.widen_bf16(xb) + orc.expert_ffn(orc.widen_bf16(u), w1[0], w3[0], w2[0])
+    assert np.max(np.abs(out - want)) < 1e-12
