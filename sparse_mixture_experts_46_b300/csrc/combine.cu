@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       uint16_t* __restrict__ y) {
   const int vec = d >> 3;
   const int64_t total = (int64_t)T * vec;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / vec);
@@ -69,9 +71,8 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<(int)blocks, 256, 0, st>>>(y_perm, slot_row, gates, residual, s.T, s.top_k,
-                                              s.dim, s.T * s.top_k, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, y_perm, slot_row,
+                    gates, residual, s.T, s.top_k, s.dim, s.T * s.top_k, y);
 }
 
 }  // namespace moe

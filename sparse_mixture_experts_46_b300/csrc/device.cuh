@@ -231,3 +231,20 @@ __device__ __forceinline__ float silu_mul(float a, float g) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// Programmatic dependent launch.  Kernels of the layer are launched with the
+// programmatic-stream-serialization attribute: a kernel may start (and run
+// its prologue) while its predecessor is still finishing, and pdl_wait()
+// blocks until the predecessor grid has completed and its writes are visible.
+// Every kernel calls pdl_wait() before its first global-memory access that
+// depends on earlier work, and writes no global memory before it.  Without
+// the attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace moe

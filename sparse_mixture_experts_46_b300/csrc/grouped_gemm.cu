@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   const int n = args.n_experts;
 
+  // Prologue independent of earlier kernels: barriers, TMEM, descriptor prefetch.
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -131,6 +132,18 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&tempty[1], 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_act);
+    tma_prefetch_desc(&tm_w0);
+    if (GLU) tma_prefetch_desc(&tm_w1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+
+  // The offsets and the activations are written by earlier kernels.
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < n; ++e) {
       const int lo = args.offsets[e];
@@ -147,12 +160,6 @@ __global__ void __launch_bounds__(192, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_act);
-    tma_prefetch_desc(&tm_w0);
-    if (GLU) tma_prefetch_desc(&tm_w1);
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -392,8 +399,7 @@ static cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& w0, const C
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(a, w0, w1, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
 }
 
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,

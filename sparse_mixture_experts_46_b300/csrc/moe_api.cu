@@ -195,12 +195,12 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* d_ids = ids ? ids : at<int32_t>(ws, L.ids);
   float* d_gates = gates ? gates : at<float>(ws, L.gates);
-  int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   uint16_t* u = norm ? at<uint16_t>(ws, L.u) : nullptr;
   const uint16_t* src = norm ? u : x;
 
-  cudaError_t e = launch_router(*shape, x, w_gate, d_ids, d_gates, counts, u,
+  // the grouping recounts the assignments from the ids: the router writes no counts
+  cudaError_t e = launch_router(*shape, x, w_gate, d_ids, d_gates, nullptr, u,
                                 norm ? opts->rmsnorm_eps : 0.0f, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_permute(*shape, src, d_ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),

@@ -14,6 +14,7 @@
 //               writing slot_row[a] and perm_src[row];
 //   4. gather:  x_perm[row] = x[perm_src[row]], 16-byte vector moves, one
 //               thread per slice.
+// For small T*K (decode batches) steps 1-3 run as one single-block kernel.
 #include "device.cuh"
 #include "internal.h"
 
@@ -24,6 +25,8 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_hist_kernel(const int32
                                                                      int32_t* __restrict__ hist) {
   __shared__ int s[kMaxExperts];
   if (threadIdx.x < kMaxExperts) s[threadIdx.x] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   const int a = blockIdx.x * kPermuteChunk + threadIdx.x;
   if (a < R) {
@@ -42,6 +45,8 @@ __global__ void __launch_bounds__(32) permute_scan_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ chunk_base) {
   const int e = threadIdx.x;
   int total = 0;
+  pdl_wait();
+  pdl_launch_dependents();
   if (e < n) {
     for (int c = 0; c < nchunks; ++c) {
       const int v = hist[(size_t)c * n + e];
@@ -73,6 +78,8 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
 
   const int a = blockIdx.x * kPermuteChunk + threadIdx.x;
@@ -100,6 +107,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           uint16_t* __restrict__ x_perm) {
   const int vec = d >> 3;
   const int64_t total = (int64_t)R * vec;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(i / vec);
@@ -111,27 +120,110 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
+// Steps 1-3 in one block of 1024 threads, for small T*K (<= kSmallPermute):
+// a shared histogram gives counts and offsets; the assignments are then
+// ranked 1024 at a time (warp match + popcount, prefix over the 32 warps, and
+// a running row base per expert carried from one 1024-slice to the next).
+constexpr int kSmallPermute = 2048;
+
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids,
+                                                            int R, int K, int n,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ perm_src,
+                                                            int32_t* __restrict__ slot_row) {
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_base[kMaxExperts];
+  __shared__ int s_wcnt[32][kMaxExperts];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  if (tid < kMaxExperts) s_cnt[tid] = 0;
+  for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();
+  for (int a = tid; a < R; a += blockDim.x) {
+    const int e = ids[a];
+    if ((unsigned)e < (unsigned)n) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int total = lane < n ? s_cnt[lane] : 0;
+    int incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane < n) {
+      s_base[lane] = incl - total;
+      offsets[lane] = incl - total;
+      if (counts) counts[lane] = total;
+    }
+    if (lane == n - 1) offsets[n] = incl;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < R; c0 += blockDim.x) {
+    const int a = c0 + tid;
+    int e = (a < R) ? ids[a] : -1;
+    if ((unsigned)e >= (unsigned)n) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (e >= 0 && lower == 0) s_wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += s_wcnt[w][e];
+      const int row = s_base[e] + before + __popc(lower);
+      slot_row[a] = row;
+      perm_src[row] = a / K;
+    }
+    __syncthreads();
+    if (tid < n) {
+      int add = 0;
+      for (int w = 0; w < 32; ++w) {
+        add += s_wcnt[w][tid];
+        s_wcnt[w][tid] = 0;
+      }
+      s_base[tid] += add;
+    }
+    __syncthreads();
+  }
+}
+
 cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
                            int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
                            uint16_t* x_perm, int nchunks, cudaStream_t st) {
   const int R = s.T * s.top_k;
-  if (nchunks > 0) {
-    permute_hist_kernel<<<nchunks, kPermuteChunk, 0, st>>>(ids, R, s.n_experts, chunk_hist);
+  cudaError_t e;
+  if (R <= kSmallPermute) {
+    e = launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, st, ids, R, s.top_k, s.n_experts,
+                   counts_out, offsets, perm_src, slot_row);
+    if (e != cudaSuccess) return e;
+  } else {
+    e = launch_pdl(permute_hist_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,
+                   s.n_experts, chunk_hist);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(32), 0, st, (const int32_t*)chunk_hist,
+                   nchunks, s.n_experts, counts_out, offsets, chunk_base);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(permute_scatter_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,
+                   s.top_k, s.n_experts, (const int32_t*)chunk_base, perm_src, slot_row);
+    if (e != cudaSuccess) return e;
   }
-  permute_scan_kernel<<<1, 32, 0, st>>>(chunk_hist, nchunks, s.n_experts, counts_out, offsets,
-                                        chunk_base);
-  if (R == 0) return cudaGetLastError();
-  permute_scatter_kernel<<<nchunks, kPermuteChunk, 0, st>>>(ids, R, s.top_k, s.n_experts,
-                                                            chunk_base, perm_src, slot_row);
+  if (R == 0) return cudaSuccess;
   if (x_perm != nullptr) {
     const int64_t total = (int64_t)R * (s.dim / 8);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(x, perm_src, R, s.dim, s.T, x_perm);
+    e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, x,
+                   (const int32_t*)perm_src, R, s.dim, s.T, x_perm);
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace moe
