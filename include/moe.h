@@ -72,9 +72,13 @@ typedef struct {
 /* Expert-FFN implementation choice (moe_layer_opts.ffn_path, and the `path`
  * argument of moe_expert_ffn_grouped). */
 enum {
-  MOE_FFN_AUTO = 0,          /* weight stream for small T, grouped GEMM otherwise */
+  MOE_FFN_AUTO = 0,          /* weight stream for T <= 32; otherwise the CTA-pair
+                                GEMM when dim % 256 == 0, else the grouped GEMM */
   MOE_FFN_GROUPED_GEMM = 1,  /* tokens on the MMA M side, 128-row token tiles */
-  MOE_FFN_WEIGHT_STREAM = 2  /* weights on the MMA M side, 32-token chunks */
+  MOE_FFN_WEIGHT_STREAM = 2, /* weights on the MMA M side, 32-token chunks */
+  MOE_FFN_PAIR_GEMM = 3      /* weights on the M side of a two-SM (CTA pair) MMA,
+                                token tiles of up to 256 rows; needs dim % 256 == 0
+                                (MOE_ERR_UNSUPPORTED_SHAPE otherwise) */
 };
 
 /* Options of moe_layer_forward; pass NULL for the plain layer. */

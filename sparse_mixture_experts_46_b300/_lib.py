@@ -26,6 +26,7 @@ MOE_ERR_TIMEOUT = 5
 MOE_FFN_AUTO = 0
 MOE_FFN_GROUPED_GEMM = 1
 MOE_FFN_WEIGHT_STREAM = 2
+MOE_FFN_PAIR_GEMM = 3
 
 # Every symbol include/moe.h declares.
 EXPORTS = (

@@ -411,6 +411,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
   const int d = s.dim, hd = s.hidden, n = s.n_experts;
   const bool stream = path == MOE_FFN_WEIGHT_STREAM ||
                       (path == MOE_FFN_AUTO && s.T <= kAutoStreamMaxT);
+  if (path == MOE_FFN_PAIR_GEMM || (path == MOE_FFN_AUTO && !stream && pair_ffn_supported(s)))
+    return launch_expert_ffn_pair(s, x_perm, offsets, w1, w3, w2, h, y_perm, err, st);
   const int grid = num_sms();
   CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
   GemmArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd};

@@ -57,6 +57,13 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
                               const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                               uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
                               cudaStream_t st);
+// CTA-pair variant (weights on the MMA M side, cta_group::2); requires
+// pair_ffn_supported(s).
+bool pair_ffn_supported(const moe_shape& s);
+cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
+                                   const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
+                                   const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
+                                   uint32_t* err, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 int num_sms();

@@ -146,7 +146,8 @@ moe_status moe_expert_ffn_grouped(const moe_shape* shape, const moe_bf16* x_perm
                                   void* ws, size_t ws_bytes, void* stream) {
   if (shape == nullptr) return MOE_ERR_INVALID_ARG;
   if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (path < MOE_FFN_AUTO || path > MOE_FFN_WEIGHT_STREAM) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_FFN_AUTO || path > MOE_FFN_PAIR_GEMM) return MOE_ERR_INVALID_ARG;
+  if (path == MOE_FFN_PAIR_GEMM && !pair_ffn_supported(*shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(w1) || !ok_ptr(w3) ||
                        !ok_ptr(w2) || !ok_ptr(h) || !ok_ptr(y_perm)))
@@ -178,7 +179,8 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
   const int path = opts ? opts->ffn_path : MOE_FFN_AUTO;
-  if (path < MOE_FFN_AUTO || path > MOE_FFN_WEIGHT_STREAM) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_FFN_AUTO || path > MOE_FFN_PAIR_GEMM) return MOE_ERR_INVALID_ARG;
+  if (path == MOE_FFN_PAIR_GEMM && !pair_ffn_supported(*shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool norm = opts && opts->use_rmsnorm;
   if (norm && !(opts->rmsnorm_eps > 0.0f)) return MOE_ERR_INVALID_ARG;
   const moe_bf16* residual = opts ? opts->residual : nullptr;

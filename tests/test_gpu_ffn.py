@@ -10,7 +10,7 @@ from tests.gpu_util import assert_bf16_close, dev_bf16, dev_i32, host_bits, lib
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"gemm": 1, "stream": 2}
+PATHS = {"gemm": 1, "stream": 2, "pair": 3}
 
 
 def ffn_case(counts, dim, hidden, seed):
@@ -80,7 +80,7 @@ def test_ffn_ragged_groups(path):
     check_ffn([0, 1, 127, 128, 129, 300, 5, 2], 128, 256, path, seed=2)
 
 
-@pytest.mark.parametrize("path", ["gemm", "stream"])
+@pytest.mark.parametrize("path", ["gemm", "stream", "pair"])
 def test_ffn_w2_256_wide_tiles(path):
     check_ffn([40, 0, 260, 7], 256, 384, path, seed=3)
 
@@ -104,3 +104,48 @@ def test_ffn_paths_agree_bitwise_structure():
     assert_bf16_close(y1, ref_y, "gemm")
     assert_bf16_close(y2, ref_y, "stream")
     assert_bf16_close(y1, orc.widen_bf16(y2), "gemm vs stream", atol=2e-2, rtol=2e-2)
+
+
+# The CTA-pair path (weights on the M side of a two-SM MMA, token tiles of up to
+# 256 rows whose MMA N shrinks to the rows left, rounded up to 16) needs dim % 256 == 0.
+
+def test_pair_single_full_tile():
+    check_ffn([256], 256, 128, "pair", seed=11)
+
+
+def test_pair_every_partial_width():
+    # last token tiles of 1, 15, 16, 17, 255, 256, 1 (257), 44 (300), 1 (513) rows
+    check_ffn([0, 1, 15, 16, 17, 255, 256, 257, 300, 513, 2], 256, 384, "pair", seed=12)
+
+
+def test_pair_many_tiles_per_pair():
+    # 4 x 8 weight tiles per expert for gate/up and 2 for down, several token tiles
+    check_ffn([700, 33, 0, 1200], 512, 1024, "pair", seed=13)
+
+
+def test_pair_long_reduction():
+    # down projection over K = 4096: the 6-stage ring wraps many times per tile
+    check_ffn([90, 300], 256, 4096, "pair", seed=14)
+
+
+def test_pair_rejects_dim_not_multiple_of_256():
+    moe = lib()
+    cfg, x_perm, offsets, w1, w3, w2 = ffn_case([10, 20], 384, 128, 15)
+    R = cfg.T
+    h = torch.empty((R, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, cfg.dim), dtype=torch.bfloat16, device="cuda")
+    ws = moe.new_workspace(cfg)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_expert_ffn_grouped(cfg, dev_bf16(x_perm), dev_i32(offsets), dev_bf16(w1),
+                                   dev_bf16(w3), dev_bf16(w2), h, y, ws, path=PATHS["pair"])
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_pair_agrees_with_token_tiles():
+    cfg, x_perm, offsets, w1, w3, w2 = ffn_case([129, 0, 511, 64], 512, 256, 16)
+    h1, y1 = run_ffn(cfg, x_perm, offsets, w1, w3, w2, "gemm")
+    h2, y2 = run_ffn(cfg, x_perm, offsets, w1, w3, w2, "pair")
+    ref_y, ref_h = orc.grouped_ffn(x_perm, offsets, w1, w3, w2)
+    assert_bf16_close(h2, ref_h, "pair hidden")
+    assert_bf16_close(y2, ref_y, "pair out")
+    assert_bf16_close(y2, orc.widen_bf16(y1), "pair vs gemm", atol=2e-2, rtol=2e-2)
