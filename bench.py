@@ -281,7 +281,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- traffic ---
 
-GEMM_SOURCES = ("grouped_gemm.cu", "device.cuh")
+GEMM_SOURCES = ("pair_gemm.cu", "device.cuh")
 
 
 def gemm_source_digest():
@@ -301,7 +301,7 @@ def recorded_traffic():
             not line.startswith("#"))
     except (OSError, ValueError):
         return None
-    if rec.get("grouped_gemm_sha") != gemm_source_digest():
+    if rec.get("gemm_sha") != gemm_source_digest():
         return None
     try:
         return int(rec["prefill_ffn_bytes_per_launch"])
