@@ -42,7 +42,10 @@ def layer_inputs(cfg):
 @pytest.mark.parametrize("T,dim,n,K", [
     (64, 128, 8, 2), (1, 128, 8, 2), (2, 256, 8, 2), (127, 128, 8, 2), (129, 384, 8, 2),
     (300, 128, 1, 1), (200, 128, 8, 8), (200, 128, 5, 3), (150, 256, 16, 2), (100, 128, 32, 4),
-    (77, 128, 12, 1)])
+    (77, 128, 12, 1),
+    # batches of >= 512 tokens take the warp router (W_g staged in shared memory)
+    (513, 256, 8, 2), (1000, 384, 5, 3), (600, 128, 16, 2), (777, 256, 12, 1),
+    (512, 128, 8, 8), (1030, 512, 16, 16), (2049, 4096, 8, 2)])
 def test_router_matches_oracle(T, dim, n, K):
     cfg = mi.Config("r", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=700 + T + n)
     x, wg = layer_inputs(cfg)
@@ -57,6 +60,15 @@ def test_router_exact_ties_go_to_lower_index():
     assert np.all(ids == np.array([0, 1]))
     assert np.all(gates == 0.5)
     assert counts.tolist() == [33, 33, 0, 0, 0, 0, 0, 0]
+
+
+def test_warp_router_exact_ties_go_to_lower_index():
+    cfg = mi.Config("tie", T=1025, dim=256, hidden=128, n_experts=16, top_k=3)
+    x = np.zeros((cfg.T, cfg.dim), np.uint16)
+    ids, gates, counts = run_router(cfg, x, mi.gen_router_weight(cfg))
+    assert np.all(ids == np.array([0, 1, 2]))
+    assert np.allclose(gates, 1.0 / 3.0, rtol=0, atol=1e-7)
+    assert counts.tolist() == [cfg.T] * 3 + [0] * 13
 
 
 def test_router_zero_tokens_clears_counts():

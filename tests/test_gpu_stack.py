@@ -86,6 +86,13 @@ def test_tiny_stack_all_tokens():
     assert excluded < cfg.T * cfg.layers // 4
 
 
+def test_stack_warp_router_all_tokens():
+    # >= 512 tokens: the RMSNorm is fused into the warp router
+    cfg = mi.CONFIGS["stack"].replace(T=640, dim=256, hidden=256, layers=3, seed=46106)
+    excluded = run_stack(cfg, np.arange(cfg.T))
+    assert excluded < cfg.T * cfg.layers // 4
+
+
 @pytest.mark.slow
 def test_full_stack_sampled_tokens():
     cfg = mi.CONFIGS["stack"]
