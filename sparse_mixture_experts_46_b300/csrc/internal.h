@@ -41,9 +41,21 @@ bool shape_supported(const moe_shape* s);
 WsLayout ws_layout(const moe_shape* s);
 
 // Launchers: return cudaSuccess or the launch error.
+// Router: ids/gates (and counts when non-null); with u_out, routes
+// u = RMSNorm(x) and writes u.  err: error word of the bounded waits (null:
+// the library's own word, reported by moe_check_error).
 cudaError_t launch_router(const moe_shape& s, const uint16_t* x, const uint16_t* wg, int32_t* ids,
                           float* gates, int32_t* counts, uint16_t* u_out, float eps,
-                          cudaStream_t st);
+                          uint32_t* err, cudaStream_t st);
+// Tensor-core router (n <= 16) and the RMSNorm kernel it is paired with.
+bool router_tc_supported(const moe_shape& s);
+cudaError_t launch_router_tc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                             int32_t* ids, float* gates, int32_t* counts, uint32_t* err,
+                             cudaStream_t st);
+cudaError_t launch_rmsnorm(const moe_shape& s, const uint16_t* x, float eps, uint16_t* u,
+                           cudaStream_t st);
+// Read (synchronously) and clear the library's router error word.
+cudaError_t router_err_read_clear(uint32_t* word);
 cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
                            int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,

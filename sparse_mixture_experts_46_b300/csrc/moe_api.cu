@@ -120,7 +120,7 @@ moe_status moe_router_topk(const moe_shape* shape, const moe_bf16* x, const moe_
   if (!ok_ptr(counts)) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(ids) || !ok_ptr(gates)))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router(*shape, x, w_gate, ids, gates, counts, nullptr, 0.0f,
+  return cuda_status(launch_router(*shape, x, w_gate, ids, gates, counts, nullptr, 0.0f, nullptr,
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -203,7 +203,7 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
 
   // the grouping recounts the assignments from the ids: the router writes no counts
   cudaError_t e = launch_router(*shape, x, w_gate, d_ids, d_gates, nullptr, u,
-                                norm ? opts->rmsnorm_eps : 0.0f, st);
+                                norm ? opts->rmsnorm_eps : 0.0f, at<uint32_t>(ws, L.err), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_permute(*shape, src, d_ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
                      at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src),
@@ -221,10 +221,12 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
 moe_status moe_check_error(void* ws, void* stream) {
   if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
+  uint32_t word = 0, router_word = 0;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (router_err_read_clear(&router_word) != cudaSuccess) return MOE_ERR_CUDA;
+  if (router_word != 0 && word == 0) return MOE_ERR_TIMEOUT;
   if (word != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)

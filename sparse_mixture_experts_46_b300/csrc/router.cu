@@ -260,211 +260,6 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(
   if (counts != nullptr && tid < n && s_hist[tid] != 0) atomicAdd(&counts[tid], s_hist[tid]);
 }
 
-// ---------------------------------------------------------------------------
-// Large-batch router: one warp owns TPW = 32 / NE consecutive tokens.
-//
-// W_g is staged once per block in shared memory as [NE/8][8][d/8] rows of 8
-// experts (16 bytes): row (q, jj, c) holds W_g[8c + jj][8q .. 8q + 7], so the
-// 32 lanes of a warp, which own consecutive 8-element slices c of the token
-// row, read consecutive 16-byte rows (no bank conflicts).  Every lane keeps
-// TPW x NE = 32 fp32 partial logits; a butterfly reduce-scatter (31 shuffles,
-// a fixed tree, deterministic) leaves lane l with the logit of token
-// t0 + l / NE and expert l % NE.  The top K are then chosen inside each group
-// of NE lanes by K argmax butterflies (strictly greater wins, ties go to the
-// lower expert index), and the gates are the softmax of the selected logits
-// in slot order.
-template <int NE>
-__global__ void __launch_bounds__(128) router_warp_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, int T, int d, int n, int K,
-    int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts,
-    uint16_t* __restrict__ u_out, float eps) {
-  constexpr int TPW = 32 / NE;
-  constexpr int NQ = NE / 8;
-  extern __shared__ __align__(16) uint4 s_w[];  // [NQ][8][d/8] rows of 8 bf16
-  __shared__ int s_hist[kMaxExperts];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int nchunks = d >> 3;
-  const bool norm = (u_out != nullptr);
-  if (tid < kMaxExperts) s_hist[tid] = 0;
-
-  pdl_wait();  // x and W_g may be written by the previous kernel
-  pdl_launch_dependents();
-  if (n == NE) {
-    // asynchronous 16-byte copies: every row of the block's share is in flight at once
-    for (int i = tid; i < d * NQ; i += blockDim.x) {
-      const int j = i % d;  // W_g row
-      const int q = i / d;  // group of 8 experts
-      const uint32_t dst = smem_u32(&s_w[(size_t)(q * 8 + (j & 7)) * nchunks + (j >> 3)]);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                   "l"(reinterpret_cast<const uint4*>(wg + (size_t)j * NE) + q)
-                   : "memory");
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  } else {
-    // n < NE: scalar loads, the padding experts get zero weights
-    for (int i = tid; i < d * NQ; i += blockDim.x) {
-      const int j = i % d;
-      const int q = i / d;
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int e0 = q * 8 + 2 * h;
-        const uint32_t lo = e0 < n ? __ldg(wg + (size_t)j * n + e0) : 0u;
-        const uint32_t hi = e0 + 1 < n ? __ldg(wg + (size_t)j * n + e0 + 1) : 0u;
-        w[h] = lo | (hi << 16);
-      }
-      s_w[(size_t)(q * 8 + (j & 7)) * nchunks + (j >> 3)] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-  __syncthreads();
-
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (tid >> 5);
-  const int nw = gridDim.x * (blockDim.x >> 5);
-  const int ngroups = (T + TPW - 1) / TPW;
-
-  // x slices of the group's TPW tokens, streamed through a PF-deep register
-  // ring: the loads of slice c + 32*PF are issued before slice c is used, so
-  // PF global loads per token are always in flight.
-  constexpr int PF = 4;
-  auto load_slice = [&](uint4* dst, int t0, int c) {
-#pragma unroll
-    for (int t = 0; t < TPW; ++t)
-      dst[t] = (c < nchunks && t0 + t < T)
-                   ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d) + c)
-                   : make_uint4(0u, 0u, 0u, 0u);
-  };
-  auto for_each_slice = [&](int t0, auto&& body) {
-    uint4 ring[PF][TPW];
-#pragma unroll
-    for (int p = 0; p < PF; ++p) load_slice(ring[p], t0, lane + 32 * p);
-    for (int base = 0; base < nchunks; base += 32 * PF) {
-#pragma unroll
-      for (int p = 0; p < PF; ++p) {
-        const int c = base + lane + 32 * p;
-        if (c < nchunks) {
-          uint4 cur[TPW];
-#pragma unroll
-          for (int t = 0; t < TPW; ++t) cur[t] = ring[p][t];
-          load_slice(ring[p], t0, c + 32 * PF);
-          body(cur, c);
-        }
-      }
-    }
-  };
-
-  for (int g = gw; g < ngroups; g += nw) {
-    const int t0 = g * TPW;
-    float rs[TPW];
-#pragma unroll
-    for (int t = 0; t < TPW; ++t) rs[t] = 1.0f;
-    if (norm) {
-      float ss[TPW];
-#pragma unroll
-      for (int t = 0; t < TPW; ++t) ss[t] = 0.0f;
-      for_each_slice(t0, [&](const uint4* cur, int) {
-#pragma unroll
-        for (int t = 0; t < TPW; ++t) {
-          float f[8];
-          unpack8(cur[t], f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ss[t] = fmaf(f[i], f[i], ss[t]);
-        }
-      });
-#pragma unroll
-      for (int t = 0; t < TPW; ++t) rs[t] = 1.0f / sqrtf(warp_sum(ss[t]) / (float)d + eps);
-    }
-
-    float acc[TPW][NE];
-#pragma unroll
-    for (int t = 0; t < TPW; ++t)
-#pragma unroll
-      for (int e = 0; e < NE; ++e) acc[t][e] = 0.0f;
-    for_each_slice(t0, [&](const uint4* cur, int c) {
-      float xv[TPW][8];
-#pragma unroll
-      for (int t = 0; t < TPW; ++t) {
-        unpack8(cur[t], xv[t]);
-        if (norm && t0 + t < T) {
-          const size_t off = (size_t)(t0 + t) * d + (size_t)c * 8;
-          uint32_t pk[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            pk[i] = pack_bf16x2(xv[t][2 * i] * rs[t], xv[t][2 * i + 1] * rs[t]);
-            xv[t][2 * i] = __uint_as_float(pk[i] << 16);
-            xv[t][2 * i + 1] = __uint_as_float(pk[i] & 0xFFFF0000u);
-          }
-          *reinterpret_cast<uint4*>(u_out + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-      }
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          float w[8];
-          unpack8(s_w[(size_t)(q * 8 + jj) * nchunks + c], w);
-#pragma unroll
-          for (int t = 0; t < TPW; ++t)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc[t][q * 8 + i] = fmaf(xv[t][jj], w[i], acc[t][q * 8 + i]);
-        }
-      }
-    });
-
-    // reduce-scatter of the 32 partial sums: lane l ends with value index l
-    float* v = &acc[0][0];
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-      const bool upper = (lane & s) != 0;
-#pragma unroll
-      for (int i = 0; i < s; ++i) {
-        const float send = upper ? v[i] : v[i + s];
-        const float keep = upper ? v[i + s] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-      }
-    }
-    const int t = t0 + lane / NE;
-    const int e = lane % NE;
-    float lv = v[0];
-    if (e >= n || !(lv == lv)) lv = -INFINITY;  // padding and NaN never beat a real logit
-
-    // top-K inside the NE-lane group; every lane follows the selection
-    float v0 = 0.0f, denom = 0.0f, mine = 0.0f;
-    int my_slot = -1;
-    float cur = lv;
-    for (int k = 0; k < K; ++k) {
-      float bv = cur;
-      int be = (my_slot < 0) ? e : kMaxExperts;  // taken lanes cannot win again
-      if (my_slot >= 0) bv = -INFINITY;
-#pragma unroll
-      for (int o = 1; o < NE; o <<= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (k == 0) v0 = bv;
-      denom += expf(bv - v0);
-      if (be == e) {
-        my_slot = k;
-        mine = bv;
-      }
-    }
-    if (t < T && my_slot >= 0) {
-      ids[(size_t)t * K + my_slot] = e;
-      gates[(size_t)t * K + my_slot] = expf(mine - v0) / denom;
-      if (counts != nullptr) atomicAdd(&s_hist[e], 1);
-    }
-  }
-  if (counts != nullptr) {
-    __syncthreads();
-    if (tid < n && s_hist[tid] != 0) atomicAdd(&counts[tid], s_hist[tid]);
-  }
-}
-
 constexpr size_t kStagedMaxBytes = 96 * 1024;
 
 template <int NE, int TPB>
@@ -488,45 +283,22 @@ static cudaError_t launch_router_t(const moe_shape& s, const uint16_t* x, const 
                     wg, s.T, s.dim, s.n_experts, s.top_k, ids, gates, counts, u_out, eps);
 }
 
-// The warp router takes batches of at least this many tokens whose W_g
-// (padded to 8 or 16 experts) fits in shared memory.
-constexpr int kWarpRouterMinT = 512;
-constexpr size_t kWarpRouterMaxBytes = 128 * 1024;
-
-template <int NE>
-static cudaError_t launch_router_warp(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                                      int32_t* ids, float* gates, int32_t* counts,
-                                      uint16_t* u_out, float eps, size_t wbytes, cudaStream_t st) {
-  auto kern = router_warp_kernel<NE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kWarpRouterMaxBytes);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, wbytes);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  const int groups = (s.T + (32 / NE) - 1) / (32 / NE);
-  int blocks = (groups + 3) / 4;  // four warps per block, one token group each
-  if (blocks > per_sm * num_sms()) blocks = per_sm * num_sms();
-  return launch_pdl(kern, dim3(blocks), dim3(128), wbytes, st, x, wg, s.T, s.dim, s.n_experts,
-                    s.top_k, ids, gates, counts, u_out, eps);
-}
-
 cudaError_t launch_router(const moe_shape& s, const uint16_t* x, const uint16_t* wg, int32_t* ids,
                           float* gates, int32_t* counts, uint16_t* u_out, float eps,
-                          cudaStream_t st) {
+                          uint32_t* err, cudaStream_t st) {
   if (counts != nullptr) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.n_experts, st);
     if (e != cudaSuccess) return e;
   }
   if (s.T == 0) return cudaSuccess;
-  if (s.T >= kWarpRouterMinT && s.n_experts <= 16) {
-    const int ne = s.n_experts <= 8 ? 8 : 16;
-    const size_t wbytes = (size_t)s.dim * ne * 2;
-    if (wbytes <= kWarpRouterMaxBytes) {
-      return ne == 8 ? launch_router_warp<8>(s, x, wg, ids, gates, counts, u_out, eps, wbytes, st)
-                     : launch_router_warp<16>(s, x, wg, ids, gates, counts, u_out, eps, wbytes, st);
+  if (router_tc_supported(s)) {
+    // tensor-core logits; the RMSNorm (if any) runs first as its own kernel
+    if (u_out != nullptr) {
+      cudaError_t e = launch_rmsnorm(s, x, eps, u_out, st);
+      if (e != cudaSuccess) return e;
+      x = u_out;
     }
+    return launch_router_tc(s, x, wg, ids, gates, counts, err, st);
   }
   if (s.n_experts <= 8) return launch_router_t<8, 4>(s, x, wg, ids, gates, counts, u_out, eps, st);
   if (s.n_experts <= 16) return launch_router_t<16, 2>(s, x, wg, ids, gates, counts, u_out, eps, st);
