@@ -84,6 +84,80 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Exclusive prefix sum of v over the threads of the block (blockDim.x a
+// multiple of 32, at most 1024); every thread must call it.  *total receives
+// the sum over the block.  s_scan: 33 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_scan, int* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_scan[warp] = incl;  // warp totals
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? s_scan[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    s_scan[lane] = wi - w;           // exclusive prefix of the warp totals
+    if (lane == 31) s_scan[32] = wi;  // block total
+  }
+  __syncthreads();
+  const int r = incl - v + s_scan[warp];
+  *total = s_scan[32];
+  __syncthreads();  // s_scan may be reused by the caller
+  return r;
+}
+
+// Tile schedule of a grouped GEMM from the device-resident offsets: expert e
+// owns rows [s_off[e], s_end[e]) (clamped into [0, rows_total]), split into
+// s_tiles[e] token tiles of `tok_tile` rows; its work units are
+// s_start[e] .. s_start[e+1] (tiles x `w_units` weight tiles, expert-major).
+// Every thread of the block calls it; s_scan is 33 ints of shared memory.
+__device__ __forceinline__ void build_tile_schedule(const int32_t* offsets, int n, int rows_total,
+                                                    int tok_tile, int w_units, int* s_off,
+                                                    int* s_end, int* s_tiles, int* s_start,
+                                                    int* s_scan) {
+  int carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int e = base + (int)threadIdx.x;
+    int units = 0;
+    if (e < n) {
+      const int lo = min(max(offsets[e], 0), rows_total);
+      const int hi = min(max(offsets[e + 1], lo), rows_total);
+      const int tt = (hi - lo + tok_tile - 1) / tok_tile;
+      s_off[e] = lo;
+      s_end[e] = hi;
+      s_tiles[e] = tt;
+      units = tt * w_units;
+    }
+    int total = 0;
+    const int ex = block_exclusive_scan(units, s_scan, &total);
+    if (e < n) s_start[e] = carry + ex;
+    carry += total;
+  }
+  if (threadIdx.x == 0) s_start[n] = carry;
+  __syncthreads();
+}
+
+// Expert owning work unit t: the largest e with s_start[e] <= t (t < s_start[n]).
+__device__ __forceinline__ int find_expert(const int* s_start, int n, int t) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 // ----------------------------------------------------------------- TMA ---
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {

@@ -53,6 +53,7 @@ struct GemmArgs {
   int w_tiles;             // weight tiles per expert
   int w_rows_per_expert;   // rows of one expert's weight matrix (hidden or dim)
   int out_ld;              // output row stride in elements
+  int rows_total;          // R: grouped rows (offsets are clamped to [0, R])
 };
 
 template <bool SWAP, bool GLU, int BN, int STAGES>
@@ -71,7 +72,8 @@ struct GemmCfg {
   static constexpr int ACT_ROWS = SWAP ? BN : 128;             // token rows per tile
   static constexpr int W_ROWS = SWAP ? 128 : (GLU ? BN / 2 : BN);  // weight rows per matrix
   static constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
-  static constexpr int AUX_BYTES = 1024;
+  // barriers and flags (1 KB), then the tile schedule: 4 tables of kMaxExperts + 1
+  static constexpr int AUX_BYTES = 1024 + 4 * (kMaxExperts + 1) * 4 + 33 * 4;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;  // + alignment slack
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
   static_assert(2 * ACC_COLS <= 512, "TMEM columns");
@@ -112,9 +114,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = tempty + 2;       // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_tile_start = abort_flag + 1;               // [kMaxExperts + 1]
-  int* s_act_tiles = s_tile_start + kMaxExperts + 1;  // [kMaxExperts]
-  int* s_off = s_act_tiles + kMaxExperts;           // [kMaxExperts + 1]
+  int* s_tile_start = reinterpret_cast<int*>(aux + 1024);  // [kMaxExperts + 1]
+  int* s_act_tiles = s_tile_start + kMaxExperts + 1;         // [kMaxExperts + 1]
+  int* s_off = s_act_tiles + kMaxExperts + 1;                // [kMaxExperts + 1]
+  int* s_end = s_off + kMaxExperts + 1;                      // [kMaxExperts + 1]
+  int* s_scan = s_end + kMaxExperts + 1;                     // [33]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -144,22 +148,11 @@ __global__ void __launch_bounds__(192, 1)
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < n; ++e) {
-      const int lo = args.offsets[e];
-      int cnt = args.offsets[e + 1] - lo;
-      if (cnt < 0) cnt = 0;
-      const int at = (cnt + C::ACT_ROWS - 1) / C::ACT_ROWS;
-      s_off[e] = lo;
-      s_act_tiles[e] = at;
-      s_tile_start[e] = acc;
-      acc += at * args.w_tiles;
-    }
-    s_off[n] = args.offsets[n];
-    s_tile_start[n] = acc;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  build_tile_schedule(args.offsets, n, args.rows_total, C::ACT_ROWS, args.w_tiles, s_off, s_end,
+                      s_act_tiles, s_tile_start, s_scan);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -169,8 +162,7 @@ __global__ void __launch_bounds__(192, 1)
   const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
 
   auto decode_tile = [&](int t, int& e, int& at, int& wt) {
-    e = 0;
-    while (t >= s_tile_start[e + 1]) ++e;
+    e = find_expert(s_tile_start, n, t);
     const int local = t - s_tile_start[e];
     const int na = s_act_tiles[e];
     wt = local / na;
@@ -271,7 +263,7 @@ __global__ void __launch_bounds__(192, 1)
       int e, at, wt;
       decode_tile(t, e, at, wt);
       const int act_row0 = s_off[e] + at * C::ACT_ROWS;
-      const int act_end = s_off[e + 1];
+      const int act_end = s_end[e];
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
       if (!SWAP) {
         const int row = act_row0 + q * 32 + lane;
@@ -415,8 +407,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
     return launch_expert_ffn_pair(s, x_perm, offsets, w1, w3, w2, h, y_perm, err, st);
   const int grid = num_sms();
   CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
-  GemmArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd};
-  GemmArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, 0, d, d};
+  GemmArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R};
+  GemmArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, 0, d, d, R};
   cudaError_t e;
   if (!stream) {
     if (!encode_2d(&tm_x, x_perm, d, R, 64, 128) ||

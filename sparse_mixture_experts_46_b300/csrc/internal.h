@@ -12,7 +12,7 @@
 
 namespace moe {
 
-constexpr int kMaxExperts = 32;
+constexpr int kMaxExperts = 256;
 constexpr int kPermuteChunk = 256;       // assignments per permute block
 constexpr int kStreamTokens = 32;        // token chunk (MMA N) of the weight stream
 constexpr int kAutoStreamMaxT = 32;      // MOE_FFN_AUTO: weight stream when T <= this
@@ -47,11 +47,16 @@ WsLayout ws_layout(const moe_shape* s);
 cudaError_t launch_router(const moe_shape& s, const uint16_t* x, const uint16_t* wg, int32_t* ids,
                           float* gates, int32_t* counts, uint16_t* u_out, float eps,
                           uint32_t* err, cudaStream_t st);
-// Tensor-core router (n <= 16) and the RMSNorm kernel it is paired with.
+// Tensor-core routers (n <= 16; 32 < n <= 256 with n % 8 == 0 and K <= 8) and
+// the RMSNorm kernel they are paired with.
 bool router_tc_supported(const moe_shape& s);
+bool router_wide_supported(const moe_shape& s);
 cudaError_t launch_router_tc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
                              int32_t* ids, float* gates, int32_t* counts, uint32_t* err,
                              cudaStream_t st);
+cudaError_t launch_router_wide(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                               int32_t* ids, float* gates, int32_t* counts, uint32_t* err,
+                               cudaStream_t st);
 cudaError_t launch_rmsnorm(const moe_shape& s, const uint16_t* x, float eps, uint16_t* u,
                            cudaStream_t st);
 // Read (synchronously) and clear the library's router error word.

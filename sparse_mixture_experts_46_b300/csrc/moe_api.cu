@@ -24,6 +24,8 @@ bool shape_supported(const moe_shape* s) {
   if (s == nullptr) return false;
   if (s->T < 0 || s->n_experts < 1 || s->n_experts > kMaxExperts) return false;
   if (s->top_k < 1 || s->top_k > s->n_experts) return false;
+  // more than 32 experts: the wide router (n a multiple of 8, K <= 8)
+  if (s->n_experts > 32 && (s->n_experts % 8 != 0 || s->top_k > 8)) return false;
   if (s->dim < 128 || s->dim % 128 != 0) return false;
   if (s->hidden < 128 || s->hidden % 128 != 0) return false;
   const int64_t R = (int64_t)s->T * s->top_k;

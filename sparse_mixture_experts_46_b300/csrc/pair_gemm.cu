@@ -71,7 +71,8 @@ struct PairCfg {
   static constexpr int ACC_COLS = 256;           // TMEM columns per accumulator buffer
   static constexpr int CHUNK = 32;               // accumulator columns per epilogue step
   static constexpr int STAGING_BYTES = CHUNK * 128 * 4;
-  static constexpr int AUX_BYTES = 1024;
+  // barriers and flags (1 KB), then the tile schedule: 4 tables of kMaxExperts + 1
+  static constexpr int AUX_BYTES = 1024 + 4 * (kMaxExperts + 1) * 4 + 33 * 4;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + AUX_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -111,10 +112,11 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* s_ok = abort_flag + 1;
-  int* s_tile_start = s_ok + 1;                       // [kMaxExperts + 1]
-  int* s_tok_tiles = s_tile_start + kMaxExperts + 1;  // [kMaxExperts]
-  int* s_off = s_tok_tiles + kMaxExperts;             // [kMaxExperts]
-  int* s_end = s_off + kMaxExperts;                   // [kMaxExperts]
+  int* s_tile_start = reinterpret_cast<int*>(aux + 1024);  // [kMaxExperts + 1]
+  int* s_tok_tiles = s_tile_start + kMaxExperts + 1;         // [kMaxExperts + 1]
+  int* s_off = s_tok_tiles + kMaxExperts + 1;                // [kMaxExperts + 1]
+  int* s_end = s_off + kMaxExperts + 1;                      // [kMaxExperts + 1]
+  int* s_scan = s_end + kMaxExperts + 1;                     // [33]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -148,21 +150,8 @@ __global__ void __launch_bounds__(192, 1)
   // The offsets and the activations are written by earlier kernels.
   pdl_wait();
   pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    // rows of expert e: [s_off[e], s_end[e]) clamped into [0, R]
-    int acc = 0;
-    for (int e = 0; e < n; ++e) {
-      const int lo = min(max(args.offsets[e], 0), args.rows_total);
-      const int hi = min(max(args.offsets[e + 1], lo), args.rows_total);
-      const int tt = (hi - lo + C::TOK_TILE - 1) / C::TOK_TILE;
-      s_off[e] = lo;
-      s_end[e] = hi;
-      s_tok_tiles[e] = tt;
-      s_tile_start[e] = acc;
-      acc += tt * args.w_tiles;
-    }
-    s_tile_start[n] = acc;
-  }
+  build_tile_schedule(args.offsets, n, args.rows_total, C::TOK_TILE, args.w_tiles, s_off, s_end,
+                      s_tok_tiles, s_tile_start, s_scan);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
@@ -174,8 +163,7 @@ __global__ void __launch_bounds__(192, 1)
 
   // tile -> expert e, weight tile wt, first token row, valid rows, MMA N
   auto decode_tile = [&](int t, int& e, int& wt, int& row0, int& rows, int& N) {
-    e = 0;
-    while (t >= s_tile_start[e + 1]) ++e;
+    e = find_expert(s_tile_start, n, t);
     const int local = t - s_tile_start[e];
     const int ntt = s_tok_tiles[e];
     wt = local / ntt;

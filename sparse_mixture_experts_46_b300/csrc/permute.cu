@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_hist_kernel(const int32
                                                                      int R, int n,
                                                                      int32_t* __restrict__ hist) {
   __shared__ int s[kMaxExperts];
-  if (threadIdx.x < kMaxExperts) s[threadIdx.x] = 0;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) s[e] = 0;
   pdl_wait();
   pdl_launch_dependents();
   __syncthreads();
@@ -34,15 +34,16 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_hist_kernel(const int32
     if ((unsigned)e < (unsigned)n) atomicAdd(&s[e], 1);  // ids outside [0, n) are ignored
   }
   __syncthreads();
-  if (threadIdx.x < n) hist[(size_t)blockIdx.x * n + threadIdx.x] = s[threadIdx.x];
+  for (int e = threadIdx.x; e < n; e += blockDim.x) hist[(size_t)blockIdx.x * n + e] = s[e];
 }
 
-// One block of 32 threads: thread e owns expert e.
-__global__ void __launch_bounds__(32) permute_scan_kernel(const int32_t* __restrict__ hist,
-                                                          int nchunks, int n,
-                                                          int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ chunk_base) {
+// One block of kMaxExperts threads: thread e owns expert e.
+__global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(const int32_t* __restrict__ hist,
+                                                                   int nchunks, int n,
+                                                                   int32_t* __restrict__ counts,
+                                                                   int32_t* __restrict__ offsets,
+                                                                   int32_t* __restrict__ chunk_base) {
+  __shared__ int s_scan[33];
   const int e = threadIdx.x;
   int total = 0;
   pdl_wait();
@@ -54,20 +55,15 @@ __global__ void __launch_bounds__(32) permute_scan_kernel(const int32_t* __restr
       total += v;
     }
   }
-  // exclusive prefix over experts (lanes >= n contribute 0)
-  int incl = total;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (e >= o) incl += v;
-  }
-  const int excl = incl - total;
+  // exclusive prefix over experts (threads >= n contribute 0)
+  int all = 0;
+  const int excl = block_exclusive_scan(total, s_scan, &all);
   if (e < n) {
     if (counts) counts[e] = total;
     offsets[e] = excl;
     for (int c = 0; c < nchunks; ++c) chunk_base[(size_t)c * n + e] += excl;
   }
-  if (e == n - 1) offsets[n] = incl;
+  if (e == 0) offsets[n] = all;
 }
 
 __global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
@@ -135,6 +131,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_base[kMaxExperts];
   __shared__ int s_wcnt[32][kMaxExperts];
+  __shared__ int s_scan[33];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -148,20 +145,16 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
     if ((unsigned)e < (unsigned)n) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
-  if (warp == 0) {
-    const int total = lane < n ? s_cnt[lane] : 0;
-    int incl = total;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+  {
+    const int total = tid < n ? s_cnt[tid] : 0;
+    int all = 0;
+    const int excl = block_exclusive_scan(total, s_scan, &all);
+    if (tid < n) {
+      s_base[tid] = excl;
+      offsets[tid] = excl;
+      if (counts) counts[tid] = total;
     }
-    if (lane < n) {
-      s_base[lane] = incl - total;
-      offsets[lane] = incl - total;
-      if (counts) counts[lane] = total;
-    }
-    if (lane == n - 1) offsets[n] = incl;
+    if (tid == 0) offsets[n] = all;
   }
   __syncthreads();
   for (int c0 = 0; c0 < R; c0 += blockDim.x) {
@@ -206,7 +199,7 @@ cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t*
     e = launch_pdl(permute_hist_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,
                    s.n_experts, chunk_hist);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(32), 0, st, (const int32_t*)chunk_hist,
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, (const int32_t*)chunk_hist,
                    nchunks, s.n_experts, counts_out, offsets, chunk_base);
     if (e != cudaSuccess) return e;
     e = launch_pdl(permute_scatter_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,

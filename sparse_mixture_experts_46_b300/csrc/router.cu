@@ -291,14 +291,15 @@ cudaError_t launch_router(const moe_shape& s, const uint16_t* x, const uint16_t*
     if (e != cudaSuccess) return e;
   }
   if (s.T == 0) return cudaSuccess;
-  if (router_tc_supported(s)) {
+  if (router_tc_supported(s) || router_wide_supported(s)) {
     // tensor-core logits; the RMSNorm (if any) runs first as its own kernel
     if (u_out != nullptr) {
       cudaError_t e = launch_rmsnorm(s, x, eps, u_out, st);
       if (e != cudaSuccess) return e;
       x = u_out;
     }
-    return launch_router_tc(s, x, wg, ids, gates, counts, err, st);
+    return router_tc_supported(s) ? launch_router_tc(s, x, wg, ids, gates, counts, err, st)
+                                  : launch_router_wide(s, x, wg, ids, gates, counts, err, st);
   }
   if (s.n_experts <= 8) return launch_router_t<8, 4>(s, x, wg, ids, gates, counts, u_out, eps, st);
   if (s.n_experts <= 16) return launch_router_t<16, 2>(s, x, wg, ids, gates, counts, u_out, eps, st);

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (tid < kMaxExperts) hist[tid] = 0;
+  for (int e = tid; e < kMaxExperts; e += kRtThreads) hist[e] = 0;
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_x);
   if (warp == 1) tmem_alloc(tmem_slot, 32);
 
@@ -294,6 +294,172 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Wide router: 32 < n <= 256 experts (fine-grained MoE, e.g. top 8 of 160).
+// W_g tiles arrive by TMA straight from its [dim, n] layout: a box of 64
+// experts x 64 features lands as 64 rows (features) of 128 bytes (experts),
+// 128-byte swizzled, i.e. the MN-major operand layout; the MMA is M=128 tokens
+// x N=round_up(n, 16) x K=16, B marked MN-major in the instruction descriptor
+// (matrix descriptor: 1024 bytes between 8-row feature groups, 8 KB between
+// 64-expert blocks).  One CTA per 128 tokens streams the whole model
+// dimension.  The epilogue thread of each token walks its n logits in
+// ascending expert order and keeps a sorted top-K list (strictly greater
+// displaces, so ties keep the lower index).
+constexpr int kRwThreads = 128;
+constexpr int kRwStages = 4;
+constexpr int kRwMaxK = 8;
+
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t addr, uint32_t lbo,
+                                                        uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+__global__ void __launch_bounds__(kRwThreads, 1)
+    router_tc_wide_kernel(const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_w, int T, int d, int n, int K,
+                          int nblk, int32_t* __restrict__ ids, float* __restrict__ gates,
+                          int32_t* __restrict__ counts, uint32_t* err, uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int stage_bytes = kRtTileBytes + nblk * 8192;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRwStages * stage_bytes);
+  uint64_t* empty = full + kRwStages;
+  uint64_t* tfull = empty + kRwStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* hist = abort_flag + 1;  // [kMaxExperts]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int tile = blockIdx.x;
+  const int kb_total = d / 64;
+  const int npad = (n + 15) & ~15;
+
+  if (tid == 0) {
+    for (int s = 0; s < kRwStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  for (int e = tid; e < kMaxExperts; e += kRwThreads) hist[e] = 0;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+
+  pdl_wait();  // x and W_g may be written by the previous kernel
+  pdl_launch_dependents();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wctl{abort_flag, err, limit_ns};
+
+  if (warp == 0 && lane == 0) {
+    for (int kb = 0; kb < kb_total; ++kb) {
+      const int s = kb % kRwStages;
+      const uint32_t ph = (uint32_t)(kb / kRwStages) & 1u;
+      if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) break;
+      uint8_t* st = ring + s * stage_bytes;
+      mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+      tma_load_2d(st, &tm_x, kb * 64, tile * 128, &full[s]);
+      for (int b = 0; b < nblk; ++b)
+        tma_load_2d(st + kRtTileBytes + b * 8192, &tm_w, b * 64, kb * 64, &full[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)npad) | (1u << 16);  // B MN-major
+    for (int kb = 0; kb < kb_total; ++kb) {
+      const int s = kb % kRwStages;
+      const uint32_t ph = (uint32_t)(kb / kRwStages) & 1u;
+      if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) break;
+      tc_fence_after_sync();
+      const uint32_t sa = smem_u32(ring + s * stage_bytes);
+      const uint32_t sb = sa + kRtTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ss(tmem, sdesc_kmajor_sw128(sa + kk * 32),
+                    sdesc_mnmajor_sw128(sb + kk * 2048, 8192, 1024), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+      mma_commit(&empty[s]);
+    }
+    mma_commit(tfull);
+  }
+  __syncwarp();
+
+  int ok = 0;
+  if (lane == 0) ok = mbar_wait(tfull, 0, wctl, kErrTimeoutEpilogue) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  const int t = tile * 128 + warp * 32 + lane;
+  if (ok) {
+    tc_fence_after_sync();
+    float tv[kRwMaxK];
+    int ti[kRwMaxK];
+#pragma unroll
+    for (int j = 0; j < kRwMaxK; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = j;
+    }
+    for (int c0 = 0; c0 < npad; c0 += 16) {
+      float v[16];
+      tmem_ld_16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);  // warp-collective
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float val = v[i];
+        int e = c0 + i;
+        if (e >= n || !(val == val)) continue;  // padding and NaN never enter
+        // insertion into the sorted list: a strictly greater value moves ahead
+#pragma unroll
+        for (int j = 0; j < kRwMaxK; ++j) {
+          if (j < K && val > tv[j]) {
+            const float fv = tv[j];
+            const int fi = ti[j];
+            tv[j] = val;
+            ti[j] = e;
+            val = fv;
+            e = fi;
+          }
+        }
+      }
+    }
+    if (t < T) {
+      const float v0 = tv[0];
+      float denom = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kRwMaxK; ++j)
+        if (j < K) denom += expf(tv[j] - v0);
+#pragma unroll
+      for (int j = 0; j < kRwMaxK; ++j) {
+        if (j < K) {
+          ids[(size_t)t * K + j] = ti[j];
+          gates[(size_t)t * K + j] = expf(tv[j] - v0) / denom;
+          if (counts != nullptr) atomicAdd(&hist[ti[j]], 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (counts != nullptr)
+    for (int e = tid; e < n; e += kRwThreads)
+      if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 // u = bf16(x / sqrt(mean(x^2) + eps)), one warp per token: the sum of squares
 // over the row (fixed lane order, warp butterfly), then the scaled row.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int T,
@@ -351,6 +517,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 rt_tensor_map_encoder() {
   return fn;
 }
 
+bool router_wide_supported(const moe_shape& s) {
+  return s.n_experts > 32 && s.n_experts <= kMaxExperts && s.n_experts % 8 == 0 &&
+         s.top_k <= kRwMaxK && s.dim % 64 == 0;
+}
+
 bool router_tc_supported(const moe_shape& s) {
   if (s.n_experts > 16 || s.dim % 64 != 0) return false;
   const int kb = s.dim / 64;
@@ -402,7 +573,7 @@ cudaError_t launch_router_tc(const moe_shape& s, const uint16_t* x, const uint16
          (tiles * split * 2 <= num_sms() || kb / split > kRtMaxKbPerCta))
     split *= 2;
   const int kb_per = kb / split;
-  const size_t fixed = 1024 + (size_t)kb_per * kRtWBytes + 128 * kRtPartStride * 4 + 1024;
+  const size_t fixed = 1024 + (size_t)kb_per * kRtWBytes + 128 * kRtPartStride * 4 + 2048;
   int stages = (int)((kRtSmemBudget - fixed) / kRtTileBytes);
   if (stages > kRtMaxStages) stages = kRtMaxStages;
   if (stages > kb_per) stages = kb_per;
@@ -427,6 +598,48 @@ cudaError_t launch_router_tc(const moe_shape& s, const uint16_t* x, const uint16
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, router_tc_kernel, tm, wg, s.T, s.dim, s.n_experts, s.top_k,
                             split, kb_per, stages, ids, gates, counts, err, kWaitLimitNs);
+}
+
+cudaError_t launch_router_wide(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                               int32_t* ids, float* gates, int32_t* counts, uint32_t* err,
+                               cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  if (err == nullptr) {
+    cudaError_t e = router_err_word(&err);
+    if (e != cudaSuccess) return e;
+  }
+  auto enc = rt_tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap tm_x, tm_w;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)s.dim, (cuuint64_t)s.T};
+    const cuuint64_t strides[1] = {(cuuint64_t)s.dim * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // W_g [dim, n]: experts are the contiguous (inner) dimension
+    const cuuint64_t dims[2] = {(cuuint64_t)s.n_experts, (cuuint64_t)s.dim};
+    const cuuint64_t strides[1] = {(cuuint64_t)s.n_experts * 2};
+    const cuuint32_t box[2] = {64, 64};
+    if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(wg), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int nblk = (s.n_experts + 63) / 64;
+  const size_t smem = 1024 + (size_t)kRwStages * (kRtTileBytes + nblk * 8192) + 2048;
+  cudaError_t e = cudaFuncSetAttribute(router_tc_wide_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (s.T + 127) / 128;
+  return launch_pdl(router_tc_wide_kernel, dim3((unsigned)tiles), dim3(kRwThreads), smem, st, tm_x,
+                    tm_w, s.T, s.dim, s.n_experts, s.top_k, nblk, ids, gates, counts, err,
+                    kWaitLimitNs);
 }
 
 cudaError_t launch_rmsnorm(const moe_shape& s, const uint16_t* x, float eps, uint16_t* u,

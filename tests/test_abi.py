@@ -65,8 +65,12 @@ def test_workspace_size_and_shape_rules(lib):
     for bad in [Shape(16, 100, 14336, 8, 2), Shape(16, 4096, 14300, 8, 2),
                 Shape(16, 4096, 14336, 33, 2), Shape(16, 4096, 14336, 8, 9),
                 Shape(16, 4096, 14336, 8, 0), Shape(-1, 4096, 14336, 8, 2),
-                Shape(1 << 20, 4096, 14336, 8, 2)]:
+                Shape(1 << 20, 4096, 14336, 8, 2), Shape(16, 4096, 14336, 257, 2),
+                Shape(16, 4096, 14336, 36, 2), Shape(16, 4096, 14336, 160, 9)]:
         assert lib.moe_workspace_bytes(ctypes.byref(bad)) == 0
+    for good in [Shape(16, 4096, 1792, 160, 8), Shape(16, 4096, 14336, 40, 1),
+                 Shape(16, 4096, 14336, 256, 8), Shape(16, 4096, 14336, 32, 32)]:
+        assert lib.moe_workspace_bytes(ctypes.byref(good)) > 0
     assert lib.moe_workspace_bytes(None) == 0
 
 

@@ -149,3 +149,13 @@ def test_pair_agrees_with_token_tiles():
     assert_bf16_close(h2, ref_h, "pair hidden")
     assert_bf16_close(y2, ref_y, "pair out")
     assert_bf16_close(y2, orc.widen_bf16(y1), "pair vs gemm", atol=2e-2, rtol=2e-2)
+
+
+def test_ffn_many_small_groups_160_experts():
+    # fine-grained MoE: 160 experts, most groups tiny or empty
+    rng = np.random.default_rng(17)
+    counts = rng.integers(0, 9, size=160)
+    counts[rng.choice(160, 40, replace=False)] = 0
+    counts[3] = 300
+    for path in ("pair", "gemm", "stream"):
+        check_ffn(counts, 256, 256, path, seed=17)

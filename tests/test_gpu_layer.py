@@ -18,10 +18,15 @@ _cache = {}
 
 
 def layer(name):
-    """Gap-filtered inputs of a named workload, uploaded once per session."""
+    """Gap-filtered inputs of a named workload (or a Config), uploaded once per session."""
+    if not isinstance(name, str):
+        cfg = name
+        name = cfg.name
+        _cache.pop(name, None)
+    else:
+        cfg = mi.CONFIGS[name]
     if name not in _cache:
         _cache.clear()
-        cfg = mi.CONFIGS[name]
         L = mi.make_layer(cfg)
         filter_x(cfg, L.x, L.wg, L.shift)
         dev = {k: dev_bf16(getattr(L, k)) for k in ("x", "wg", "w1", "w3", "w2")}
@@ -71,6 +76,7 @@ def fused(cfg, dev, path):
 
 def check_layer(name, path, sample=None):
     cfg, L, dev = layer(name)
+    name = cfg.name
     got = stepwise(cfg, dev, path)
     # routing: every token, bit-exact
     r_ids, r_gates, _ = orc.router(L.x, L.wg, cfg.top_k)
@@ -114,3 +120,15 @@ def test_skewed_routing_layer():
     share = np.bincount(ids[:, 0], minlength=8) / cfg.T
     assert 0.36 < share[0] < 0.50            # Zipf(1.2) top-1 share of the largest expert
     check_layer("skew", 0, sample=48)
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_fine_grained_layer_160_experts_top8(path):
+    # "routing to, for example, 8 out of 160 much smaller experts"
+    cfg = mi.Config("fine-small", T=600, dim=256, hidden=256, n_experts=160, top_k=8, seed=46107)
+    check_layer(cfg, path)
+
+
+def test_fine_grained_layer_full_dims_sampled():
+    cfg = mi.CONFIGS["fine"].replace(T=1024)
+    check_layer(cfg, 0, sample=32)

@@ -47,7 +47,8 @@ def random_ids(rng, T, n, K, weights=None):
 
 
 @pytest.mark.parametrize("T,n,K", [(1, 8, 2), (64, 8, 2), (129, 8, 2), (1000, 8, 2),
-                                   (3000, 8, 2), (257, 1, 1), (300, 8, 8), (555, 32, 3)])
+                                   (3000, 8, 2), (257, 1, 1), (300, 8, 8), (555, 32, 3),
+                                   (100, 64, 6), (300, 256, 8), (2000, 160, 8), (5, 160, 8)])
 def test_permute_matches_counting_sort(T, n, K):
     rng = np.random.default_rng(T * 31 + n)
     cfg = mi.Config("p", T=T, dim=128, hidden=128, n_experts=n, top_k=K, seed=900 + T)

@@ -45,7 +45,10 @@ def layer_inputs(cfg):
     (77, 128, 12, 1),
     # batches of >= 512 tokens take the warp router (W_g staged in shared memory)
     (513, 256, 8, 2), (1000, 384, 5, 3), (600, 128, 16, 2), (777, 256, 12, 1),
-    (512, 128, 8, 8), (1030, 512, 16, 16), (2049, 4096, 8, 2)])
+    (512, 128, 8, 8), (1030, 512, 16, 16), (2049, 4096, 8, 2),
+    # more than 32 experts (fine-grained MoE): the wide tensor-core router
+    (200, 256, 40, 2), (1000, 512, 64, 6), (700, 256, 160, 8), (129, 128, 256, 8),
+    (1, 256, 160, 8), (64, 128, 48, 1), (600, 4096, 160, 8)])
 def test_router_matches_oracle(T, dim, n, K):
     cfg = mi.Config("r", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=700 + T + n)
     x, wg = layer_inputs(cfg)
@@ -69,6 +72,15 @@ def test_warp_router_exact_ties_go_to_lower_index():
     assert np.all(ids == np.array([0, 1, 2]))
     assert np.allclose(gates, 1.0 / 3.0, rtol=0, atol=1e-7)
     assert counts.tolist() == [cfg.T] * 3 + [0] * 13
+
+
+def test_wide_router_exact_ties_go_to_lower_index():
+    cfg = mi.Config("tie", T=300, dim=256, hidden=128, n_experts=160, top_k=8)
+    x = np.zeros((cfg.T, cfg.dim), np.uint16)
+    ids, gates, counts = run_router(cfg, x, mi.gen_router_weight(cfg))
+    assert np.all(ids == np.arange(8))
+    assert np.allclose(gates, 1.0 / 8.0, rtol=0, atol=1e-7)
+    assert counts.tolist() == [cfg.T] * 8 + [0] * 152
 
 
 def test_router_zero_tokens_clears_counts():

@@ -90,6 +90,25 @@ def test_topk_brute_force_all_subsets():
                 assert sl[k] > sl[k + 1] or (sl[k] == sl[k + 1] and ids[t, k] < ids[t, k + 1])
 
 
+def test_topk_many_experts_by_pairwise_counting():
+    """Fine-grained routing (top 8 of 160, the pages' example): expert e is in
+    slot k exactly when k experts beat it, where j beats e if its logit is
+    larger or equal with a lower index (an O(n^2) restatement of the order,
+    independent of the oracle's sort)."""
+    rng = np.random.default_rng(4)
+    for n, K in [(160, 8), (64, 6), (256, 8), (40, 1)]:
+        logits = rng.integers(-6, 7, size=(60, n)).astype(np.float64)  # many exact ties
+        ids = orc.topk_order(logits)[:, :K]
+        for t in range(logits.shape[0]):
+            l = logits[t]
+            beaten_by = ((l[None, :] > l[:, None]) |
+                         ((l[None, :] == l[:, None]) & (np.arange(n)[None, :] < np.arange(n)[:, None])))
+            rank = beaten_by.sum(1)            # experts that beat e
+            expect = np.argsort(rank)[:K]      # ranks are a permutation of 0..n-1
+            assert np.array_equal(ids[t], expect)
+            assert np.array_equal(rank[ids[t]], np.arange(K))
+
+
 def test_forced_tie_goes_to_lower_index():
     x = np.zeros((3, 16))
     wg = np.random.default_rng(2).standard_normal((16, 8))
@@ -190,7 +209,7 @@ def _dense_masked_reference(x, wg, w1, w3, w2, K):
     return out
 
 
-@pytest.mark.parametrize("n,K", [(8, 2), (8, 1), (4, 3), (8, 8), (1, 1)])
+@pytest.mark.parametrize("n,K", [(8, 2), (8, 1), (4, 3), (8, 8), (1, 1), (160, 8)])
 def test_sparse_equals_dense_masked_sum(n, K):
     rng = np.random.default_rng(10 + n * 10 + K)
     x, wg, w1, w3, w2 = _rand_layer(rng, 24, 16, 12, n)
