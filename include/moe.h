@@ -26,8 +26,10 @@
  *   selected logits (float32).  The grouped ("permuted") row order is the
  *   stable sort of the flat assignments a = t*K + k by expert id: rows
  *   [offsets[e], offsets[e+1]) belong to expert e, tokens ascending.
- * - Supported shapes: T >= 0 (T = 0 is a no-op), 1 <= top_k <= n_experts <= 32,
- *   dim and hidden positive multiples of 128, T*top_k*max(dim, hidden) < 2^31.
+ * - Supported shapes: T >= 0 (T = 0 is a no-op), 1 <= top_k <= n_experts <= 256,
+ *   with n_experts a multiple of 8 and top_k <= 8 when n_experts > 32 (the
+ *   fine-grained variant: e.g. the top 8 of 160 smaller experts); dim and
+ *   hidden positive multiples of 128; T*top_k*max(dim, hidden) < 2^31.
  * - Errors: argument and shape checks return synchronously (nothing is
  *   enqueued); a failed launch returns MOE_ERR_CUDA.  Kernels never trap:
  *   a bounded device-side wait that expires records MOE_ERR_TIMEOUT in the

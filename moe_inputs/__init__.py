@@ -191,6 +191,8 @@ CONFIGS = {
     # fine-grained MoE (top 8 of 160 experts); the expert size is a reading:
     # 1/8 of a Mixtral expert, so the 8 selected experts cost one Mixtral expert
     "fine": Config("fine", T=4096, dim=4096, hidden=1792, n_experts=160, top_k=8, seed=46006),
+    "fine_decode": Config("fine_decode", T=16, dim=4096, hidden=1792, n_experts=160, top_k=8,
+                          seed=46007),
     "stack": Config("stack", T=8192, dim=4096, hidden=14336, seed=46005, layers=32,
                     rmsnorm_eps=1e-5),
 }
