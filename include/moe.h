@@ -99,8 +99,11 @@ MOE_API const char* moe_status_string(moe_status status);
  * an unsupported shape. */
 MOE_API size_t moe_workspace_bytes(const moe_shape* shape);
 
-/* Clear the workspace error word.  Call once after allocating a workspace
- * (and it is what moe_check_error leaves behind). */
+/* Prepare a workspace: zero its first 64 KB (the error word and the arrival
+ * counters of the weight stream's split tiles, which every completed call
+ * leaves at zero).  Call once after allocating a workspace, and again after
+ * moe_check_error has reported MOE_ERR_TIMEOUT (an aborted call may leave
+ * counters behind). */
 MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Router: logits l = x . w_gate in fp32 from bf16 inputs, top-K selection and

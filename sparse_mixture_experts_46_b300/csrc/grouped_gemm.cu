@@ -337,6 +337,308 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Weight stream, stream-K schedule (small T).  The weight tiles of one pass
+// (expert x 128 weight rows, over the whole reduction) do not divide evenly
+// into the SMs (e.g. 896 gate/up tiles on 148 SMs is 6.05 tiles each), and
+// the pass is HBM-bound, so a whole-tile round robin leaves most SMs idle in
+// the last round.  Here the pass is a list of units (tile, 64-wide K block)
+// and CTA c streams the contiguous units [c*U/G, (c+1)*U/G): every SM moves
+// the same number of weight bytes.  A tile that a CTA covers completely gets
+// the usual epilogue.  A tile split between CTAs: every contributor writes its
+// fp32 accumulator slice to its partial slot in the workspace, publishes it
+// (fence, then an atomic increment of the tile's counter), and the contributor
+// that arrives last sums all slices in CTA order (a fixed order:
+// deterministic), applies the epilogue and resets the counter to zero.  No CTA
+// waits for another.
+struct StreamKArgs {
+  const int32_t* offsets;  // [n + 1] grouped-row offsets (device)
+  uint16_t* out;           // H [R, hidden] (gate/up) or y_perm [R, dim] (down)
+  uint32_t* err;           // workspace error word
+  uint64_t limit_ns;       // bounded-wait limit
+  int n_experts;
+  int k_blocks;            // reduction length / 64
+  int w_tiles;             // weight tiles (128 rows) per expert
+  int w_rows_per_expert;   // rows of one expert's weight matrix
+  int out_ld;              // output row stride in elements
+  int rows_total;          // R
+  float* partials;         // [gridDim][2][128][ACC_COLS] fp32 accumulator slices
+  int* counters;           // [tiles] arrivals per split tile; zero on entry and exit
+};
+
+template <bool GLU, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    stream_k_kernel(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_w0,
+                    const __grid_constant__ CUtensorMap tm_w1, const StreamKArgs args) {
+  using C = GemmCfg<true, GLU, kStreamTokens, STAGES>;
+  constexpr int BN = kStreamTokens;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* aux = tiles + STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;       // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_ok = abort_flag + 1;   // [2] wait decisions, alternating by segment
+  int* s_last = s_ok + 2;       // last-arriver flag of the current split tile
+  int* s_tile_start = reinterpret_cast<int*>(aux + 1024);  // [kMaxExperts + 1]
+  int* s_act_tiles = s_tile_start + kMaxExperts + 1;
+  int* s_off = s_act_tiles + kMaxExperts + 1;
+  int* s_end = s_off + kMaxExperts + 1;
+  int* s_scan = s_end + kMaxExperts + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n = args.n_experts;
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_act);
+    tma_prefetch_desc(&tm_w0);
+    if (GLU) tma_prefetch_desc(&tm_w1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  build_tile_schedule(args.offsets, n, args.rows_total, C::ACT_ROWS, args.w_tiles, s_off, s_end,
+                      s_act_tiles, s_tile_start, s_scan);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int KB = args.k_blocks;
+  const int64_t U = (int64_t)s_tile_start[n] * KB;  // units of the pass
+  auto range_start = [&](int c) -> int64_t { return (int64_t)c * U / G; };
+  const int64_t u0 = range_start(cta), u1 = range_start(cta + 1);
+  const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
+
+  auto decode_tile = [&](int t, int& e, int& at, int& wt) {
+    e = find_expert(s_tile_start, n, t);
+    const int local = t - s_tile_start[e];
+    const int na = s_act_tiles[e];
+    wt = local / na;
+    at = local - wt * na;
+  };
+  // segments of this CTA's range: tile t, K blocks [kb_lo, kb_hi)
+  const int t_first = u0 < u1 ? (int)(u0 / KB) : 0;
+  const int t_stop = u0 < u1 ? (int)((u1 - 1) / KB) + 1 : 0;
+  auto seg_bounds = [&](int t, int& kb_lo, int& kb_hi) {
+    const int64_t base = (int64_t)t * KB;
+    kb_lo = u0 > base ? (int)(u0 - base) : 0;
+    kb_hi = u1 < base + KB ? (int)(u1 - base) : KB;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer ---
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = t_first; ok && t < t_stop; ++t) {
+        int e, at, wt, kb_lo, kb_hi;
+        decode_tile(t, e, at, wt);
+        seg_bounds(t, kb_lo, kb_hi);
+        const int act_row = s_off[e] + at * C::ACT_ROWS;
+        const int w_row = e * args.w_rows_per_expert + wt * C::W_ROWS;
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          const int kx = kb * C::BK;
+          tma_load_2d(st, &tm_w0, kx, w_row, &full[s]);
+          if (GLU) tma_load_2d(st + C::A_BYTES, &tm_w1, kx, w_row, &full[s]);
+          tma_load_2d(st + C::NUM_A * C::A_BYTES, &tm_act, kx, act_row, &full[s]);
+        }
+      }
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        drain_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, args.err, args.limit_ns);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = t_first; ok && t < t_stop; ++t, ++lt) {
+        int kb_lo, kb_hi;
+        seg_bounds(t, kb_lo, kb_hi);
+        const int b = lt & 1;
+        const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + (uint32_t)(b * C::ACC_COLS);
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(tiles + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::NUM_A * C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
+            mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
+                        C::IDESC, accum);
+            if (GLU)
+              mma_bf16_ss(d0 + BN, sdesc_kmajor_sw128(sa + C::A_BYTES + kk * 32),
+                          sdesc_kmajor_sw128(sb + kk * 32), C::IDESC, accum);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tfull[b]);
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0, args.err, args.limit_ns);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue ---
+    const int q = warp & 3;            // this warp's TMEM lane quarter
+    const int et = threadIdx.x - 64;   // 0..127
+    const int r = q * 32 + lane;       // accumulator row (weight row inside the tile)
+    auto cta_of_unit = [&](int64_t u) {
+      int c = (int)(u * G / U);
+      while (c + 1 < G && range_start(c + 1) <= u) ++c;
+      while (c > 0 && range_start(c) > u) --c;
+      return c;
+    };
+    int lt = 0;
+    for (int t = t_first; t < t_stop; ++t, ++lt) {
+      const int b = lt & 1;
+      const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+      // one thread decides for all four warps (they then meet the same barriers);
+      // the decision slot alternates so the next write cannot overtake a read
+      if (et == 0) s_ok[b] = mbar_wait(&tfull[b], tph, wctl, kErrTimeoutEpilogue) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!s_ok[b]) break;
+      tc_fence_after_sync();
+      int e, at, wt, kb_lo, kb_hi;
+      decode_tile(t, e, at, wt);
+      seg_bounds(t, kb_lo, kb_hi);
+      const int act_row0 = s_off[e] + at * C::ACT_ROWS;
+      const int act_end = s_end[e];
+      const int j = wt * 128 + r;  // output column
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      float acc[C::ACC_COLS];
+#pragma unroll
+      for (int c = 0; c < C::ACC_COLS; c += 32) {
+        float v0[16], v1[16];
+        tmem_ld_2x16(tacc + c, tacc + c + 16, v0, v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          acc[c + i] = v0[i];
+          acc[c + 16 + i] = v1[i];
+        }
+      }
+      bool emit = (kb_lo == 0 && kb_hi == KB);  // this CTA covers the whole tile
+      if (!emit) {
+        // publish this CTA's slice, then count the arrival
+        const int64_t base = (int64_t)t * KB;
+        const int slot = u0 > base ? 0 : 1;
+        float4* dst = reinterpret_cast<float4*>(
+            args.partials + ((size_t)(cta * 2 + slot) * 128 + r) * C::ACC_COLS);
+#pragma unroll
+        for (int c = 0; c < C::ACC_COLS; c += 4)
+          dst[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        // contributors: the CTAs from the one holding the tile's first unit to the
+        // one holding its last, skipping those whose range is empty
+        const int c_first = cta_of_unit(base), c_last = cta_of_unit(base + KB - 1);
+        if (et == 0) {
+          int parts = 0;
+          int64_t lo = range_start(c_first);
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            const int64_t hi = range_start(cc + 1);
+            parts += hi > lo ? 1 : 0;
+            lo = hi;
+          }
+          const int old = atomicAdd(&args.counters[t], 1);
+          *s_last = (old == parts - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        emit = *s_last != 0;
+        if (emit) {
+          __threadfence();
+          // every contributor's slice, in CTA order
+#pragma unroll
+          for (int c = 0; c < C::ACC_COLS; ++c) acc[c] = 0.0f;
+          int64_t lo = range_start(c_first);
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            const int64_t hi = range_start(cc + 1);
+            const bool contributes = hi > lo;
+            const int sl = lo > base ? 0 : 1;
+            lo = hi;
+            if (!contributes) continue;
+            const float4* src = reinterpret_cast<const float4*>(
+                args.partials + ((size_t)(cc * 2 + sl) * 128 + r) * C::ACC_COLS);
+#pragma unroll
+            for (int c = 0; c < C::ACC_COLS; c += 4) {
+              const float4 v = __ldcg(src + c / 4);
+              acc[c] += v.x;
+              acc[c + 1] += v.y;
+              acc[c + 2] += v.z;
+              acc[c + 3] += v.w;
+            }
+          }
+          if (et == 0) args.counters[t] = 0;  // ready for the next call
+        }
+      }
+      if (emit) {
+        // lane <-> weight row j (output column); accumulator columns <-> token rows
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int row = act_row0 + i;
+          if (row < act_end) {
+            const float v = GLU ? silu_mul(acc[i], acc[BN + i]) : acc[i];
+            const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+            args.out[(size_t)row * args.out_ld + j] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
 __global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -394,10 +696,22 @@ static cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& w0, const C
   return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
 }
 
+template <bool GLU, int STAGES>
+static cudaError_t run_stream_k(const CUtensorMap& a, const CUtensorMap& w0,
+                                const CUtensorMap& w1, const StreamKArgs& args, int grid,
+                                cudaStream_t st) {
+  using C = GemmCfg<true, GLU, kStreamTokens, STAGES>;
+  auto kern = stream_k_kernel<GLU, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
+}
+
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
                               const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                               uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
-                              cudaStream_t st) {
+                              float* partials, int* counters, cudaStream_t st) {
   const int R = s.T * s.top_k;
   if (R == 0) return cudaSuccess;
   const int d = s.dim, hd = s.hidden, n = s.n_experts;
@@ -433,6 +747,20 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
       !encode_2d(&tm_h, h, hd, R, 64, kStreamTokens) ||
       !encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 64, 128))
     return cudaErrorInvalidValue;
+  // stream-K when the tiles of a pass surely fit the counters: an expert with
+  // c rows has ceil(c / 32) token tiles, so a pass has at most
+  // (R / 32 + n) * (weight tiles per expert) tiles
+  const int64_t max_tiles = ((int64_t)R / kStreamTokens + n) * ((d > hd ? d : hd) / 128);
+  if (partials != nullptr && counters != nullptr && max_tiles <= kStreamKCounters &&
+      grid <= kStreamKMaxCtas) {
+    const StreamKArgs k1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R,
+                         partials, counters};
+    e = run_stream_k<true, 6>(tm_x, tm_w1, tm_w3, k1, grid, st);
+    if (e != cudaSuccess) return e;
+    const StreamKArgs k2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 128, d, d, R,
+                         partials, counters};
+    return run_stream_k<false, 10>(tm_h, tm_w2, tm_w2, k2, grid, st);
+  }
   e = run_gemm<true, true, kStreamTokens, 6>(tm_x, tm_w1, tm_w3, a1, grid, st);
   if (e != cudaSuccess) return e;
   a2.w_tiles = d / 128;

@@ -44,7 +44,8 @@ WsLayout ws_layout(const moe_shape* s) {
   L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
   size_t off = 0;
   L.err = off;
-  off += 4096;  // header page
+  L.counters = kWsHeaderBytes;
+  off += kWsControlBytes;  // control region: error word, stream-K counters
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off = align_up(off + bytes);
@@ -62,6 +63,7 @@ WsLayout ws_layout(const moe_shape* s) {
   L.x_perm = take(R * (size_t)s->dim * 2);
   L.h = take(R * (size_t)s->hidden * 2);
   L.y_perm = take(R * (size_t)s->dim * 2);
+  L.partials = take((size_t)kStreamKMaxCtas * 2 * 128 * 64 * 4);
   L.total = off;
   return L;
 }
@@ -111,8 +113,9 @@ size_t moe_workspace_bytes(const moe_shape* shape) {
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
-  if (!ok_ptr(ws) || ws_bytes < 4096) return MOE_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(ws, 0, 4096, static_cast<cudaStream_t>(stream)));
+  if (!ok_ptr(ws) || ws_bytes < kWsHeaderBytes) return MOE_ERR_INVALID_ARG;
+  const size_t n = ws_bytes < kWsControlBytes ? ws_bytes : kWsControlBytes;
+  return cuda_status(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_router_topk(const moe_shape* shape, const moe_bf16* x, const moe_bf16* w_gate,
@@ -157,7 +160,8 @@ moe_status moe_expert_ffn_grouped(const moe_shape* shape, const moe_bf16* x_perm
   const WsLayout L = ws_layout(shape);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const cudaError_t e = launch_expert_ffn(*shape, x_perm, offsets, w1, w3, w2, h, y_perm, path,
-                                          at<uint32_t>(ws, L.err),
+                                          at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
+                                          at<int>(ws, L.counters),
                                           static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
@@ -213,7 +217,8 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_expert_ffn(*shape, at<uint16_t>(ws, L.x_perm), offsets, w1, w3, w2,
                         at<uint16_t>(ws, L.h), at<uint16_t>(ws, L.y_perm), path,
-                        at<uint32_t>(ws, L.err), st);
+                        at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
+                        at<int>(ws, L.counters), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_combine(*shape, at<uint16_t>(ws, L.y_perm), at<int32_t>(ws, L.slot_row), d_gates,
                      residual, y, st);

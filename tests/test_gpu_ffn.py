@@ -159,3 +159,35 @@ def test_ffn_many_small_groups_160_experts():
     counts[3] = 300
     for path in ("pair", "gemm", "stream"):
         check_ffn(counts, 256, 256, path, seed=17)
+
+
+# The weight stream splits each pass into equal ranges of (tile, K block) units
+# over the SMs (stream-K); tiles split between CTAs are summed by the last one.
+
+def test_stream_k_tile_split_over_many_ctas():
+    # one expert, 5 rows: the down pass has 2 weight tiles of 32 K blocks each,
+    # so every tile is shared by ~74 CTAs; gate/up has 16 tiles of 4 K blocks
+    check_ffn([5], 256, 2048, "stream", seed=21)
+
+
+def test_stream_k_counters_return_to_zero():
+    """Three calls on one workspace give identical bits (every split tile's
+    arrival counter is back at zero after each call)."""
+    moe = lib()
+    cfg, x_perm, offsets, w1, w3, w2 = ffn_case([3, 0, 17, 9, 30, 1], 256, 640, 22)
+    R = cfg.T
+    ws = moe.new_workspace(cfg)
+    args = [dev_bf16(x_perm), dev_i32(offsets), dev_bf16(w1), dev_bf16(w3), dev_bf16(w2)]
+    outs = []
+    for _ in range(3):
+        h = torch.full((R, cfg.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((R, cfg.dim), float("nan"), dtype=torch.bfloat16, device="cuda")
+        moe.moe_expert_ffn_grouped(cfg, args[0], args[1], args[2], args[3], args[4], h, y, ws,
+                                   path=PATHS["stream"])
+        assert moe.moe_check_error(ws) == moe.MOE_OK
+        outs.append((host_bits(h), host_bits(y)))
+    ref_y, ref_h = orc.grouped_ffn(x_perm, offsets, w1, w3, w2)
+    assert_bf16_close(outs[0][0], ref_h, "hidden activations")
+    assert_bf16_close(outs[0][1], ref_y, "expert outputs")
+    for h, y in outs[1:]:
+        assert np.array_equal(h, outs[0][0]) and np.array_equal(y, outs[0][1])
