@@ -159,6 +159,21 @@ MOE_API moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opt
                              float* gates, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* Routing statistics ("Mixtral of Experts" section 5, Routing analysis) of
+ * the expert ids [T, K] produced by moe_router_topk or moe_layer_forward:
+ *   slot_counts [K * n]  slot_counts[k*n + e] = tokens whose k-th choice is
+ *                        expert e (Fig. 7 shares: sum over k divided by T*K;
+ *                        Fig. 9: per k divided by T);
+ *   repeats [2]          repeats[0] = pairs of consecutive tokens (t, t+1)
+ *                        with the same first choice; repeats[1] = pairs whose
+ *                        K chosen experts share at least one expert (Table 5,
+ *                        "first choice only" and "first or second choice";
+ *                        divide by T-1 for the rates).
+ * Both outputs are zeroed and filled by this call (integer counts: exact and
+ * independent of scheduling).  Ids outside [0, n) are not counted. */
+MOE_API moe_status moe_routing_stats(const moe_shape* shape, const int32_t* ids,
+                                     int32_t* slot_counts, int32_t* repeats, void* stream);
+
 /* Synchronise `stream`, read and clear the workspace error word.  Returns
  * MOE_ERR_TIMEOUT if any bounded device wait expired since the last check,
  * MOE_ERR_CUDA on a pending CUDA error, MOE_OK otherwise. */

@@ -200,6 +200,35 @@ def routing_tables(ids: np.ndarray, n_experts: int):
     return counts, offsets, perm_src, slot_row
 
 
+def routing_stats(ids: np.ndarray, n_experts: int):
+    """Routing statistics of "Mixtral of Experts" section 5 (Routing analysis).
+
+    slot_counts[k, e]  tokens whose k-th choice is expert e (Fig. 7 counts the
+                       first or second choice, i.e. the sum over k; Fig. 9
+                       splits it by choice);
+    first_repeat       pairs of consecutive tokens (t, t+1) with the same first
+                       choice (Table 5, "first choice only");
+    any_repeat         pairs whose sets of K chosen experts share at least one
+                       expert (Table 5, "first or second choice" for K = 2);
+    pairs              T - 1 consecutive pairs (0 when T < 2).
+    """
+    ids = np.asarray(ids)
+    T, K = ids.shape
+    slot_counts = np.zeros((K, n_experts), dtype=np.int64)
+    for k in range(K):
+        for t in range(T):
+            slot_counts[k, ids[t, k]] += 1
+    first_repeat = 0
+    any_repeat = 0
+    for t in range(T - 1):
+        if ids[t, 0] == ids[t + 1, 0]:
+            first_repeat += 1
+        if set(ids[t].tolist()) & set(ids[t + 1].tolist()):
+            any_repeat += 1
+    return dict(slot_counts=slot_counts, first_repeat=first_repeat, any_repeat=any_repeat,
+                pairs=max(T - 1, 0))
+
+
 def grouped_ffn(x_perm, offsets, w1, w3, w2, h_bf16: bool = False):
     """Expert FFN over grouped rows: rows [offsets[e], offsets[e+1]) use expert e.
 

@@ -32,7 +32,7 @@ MOE_FFN_PAIR_GEMM = 3
 EXPORTS = (
     "moe_status_string", "moe_workspace_bytes", "moe_workspace_init", "moe_router_topk",
     "moe_permute", "moe_expert_ffn_grouped", "moe_combine", "moe_layer_forward",
-    "moe_check_error", "moe_selftest_wait_timeout", "moe_permute_noalloc",
+    "moe_check_error", "moe_selftest_wait_timeout", "moe_permute_noalloc", "moe_routing_stats",
 )
 
 
@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "moe_check_error": (i32, [vp, vp]),
         "moe_selftest_wait_timeout": (i32, [vp, sz, ctypes.c_uint64, vp]),
         "moe_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
+        "moe_routing_stats": (i32, [sp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -190,6 +191,14 @@ def moe_combine(shape, y_perm, slot_row, gates, y, residual=None, stream=None) -
                             _ptr(slot_row, _I32, "slot_row"), _ptr(gates, _F32, "gates"),
                             _ptr(residual, _BF16, "residual", nullable=True),
                             _ptr(y, _BF16, "y"), _stream(stream)), "moe_combine")
+
+
+def moe_routing_stats(shape, ids, slot_counts, repeats, stream=None) -> None:
+    s = _shape(shape)
+    _check(_LIB.moe_routing_stats(ctypes.byref(s), _ptr(ids, _I32, "ids"),
+                                  _ptr(slot_counts, _I32, "slot_counts"),
+                                  _ptr(repeats, _I32, "repeats"), _stream(stream)),
+           "moe_routing_stats")
 
 
 def moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, ids=None, gates=None,

@@ -93,6 +93,9 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
                                    const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
                                    const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
                                    uint32_t* err, cudaStream_t st);
+// Routing statistics (slot_counts [K * n], repeats [2]); zeroes both first.
+cudaError_t launch_routing_stats(const moe_shape& s, const int32_t* ids, int32_t* slot_counts,
+                                 int32_t* repeats, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 int num_sms();

@@ -225,6 +225,16 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   return cuda_status(e);
 }
 
+moe_status moe_routing_stats(const moe_shape* shape, const int32_t* ids, int32_t* slot_counts,
+                             int32_t* repeats, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ok_ptr(slot_counts) || !ok_ptr(repeats)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && !ok_ptr(ids)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_routing_stats(*shape, ids, slot_counts, repeats,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_check_error(void* ws, void* stream) {
   if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -303,6 +303,28 @@ def test_random_routing_matches_printed_expectations():
     assert abs(either - exp_either) < 0.025
 
 
+def test_routing_stats_hand_example_and_random_expectations():
+    """Table 5 statistics: a hand-worked sequence, then iid tokens against the
+    printed random expectations (12.5 % first choice, 1-(6/8)(5/7) ~ 46 %)."""
+    ids = np.array([[0, 1], [0, 2], [3, 1], [4, 5], [5, 4], [5, 6]])
+    st = orc.routing_stats(ids, 8)
+    # pairs (0,1): same first choice; (1,2): no shared expert; (2,3): none;
+    # (3,4): share 4 and 5; (4,5): same first choice 5
+    assert st["pairs"] == 5
+    assert st["first_repeat"] == 2
+    assert st["any_repeat"] == 3
+    assert st["slot_counts"][0].tolist() == [2, 0, 0, 1, 1, 2, 0, 0]
+    assert st["slot_counts"][1].tolist() == [0, 2, 1, 0, 1, 1, 1, 0]
+    g = _golden("routing_random_expectations.json")
+    rng = np.random.default_rng(5)
+    ids = np.stack([rng.permutation(8)[:2] for _ in range(20000)])
+    st = orc.routing_stats(ids, 8)
+    assert abs(st["first_repeat"] / st["pairs"] - g["first_choice_repeat"]) < 0.01
+    assert abs(st["any_repeat"] / st["pairs"] - (1 - (6 / 8) * (5 / 7))) < 0.015
+    share = st["slot_counts"].sum(0) / ids.size
+    assert np.all(np.abs(share - g["uniform_share"]) < 0.01)
+
+
 def test_stack_layer_residual_and_zero_experts():
     """x + MoE(RMSNorm(x)): with W2 = 0 every expert outputs 0, so the block is the
     identity; with identical experts it is x + FFN(RMSNorm(x))."""
