@@ -164,6 +164,65 @@ def moe_layer(x, w_gate, w1, w3, w2, top_k: int, h_bf16: bool = False):
     return y, ids, gates
 
 
+def silu_grad(a: np.ndarray) -> np.ndarray:
+    """d SiLU / da = sigmoid(a) * (1 + a * (1 - sigmoid(a)))."""
+    sg = 1.0 / (1.0 + np.exp(-a))
+    return sg * (1.0 + a * (1.0 - sg))
+
+
+def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy):
+    """Gradients of the sparse MoE layer (§2.1) for an upstream gradient dy.
+
+    The routing (which K experts each token uses) is held fixed: TopK is
+    piecewise constant, so the gradient reaches W_g and x only through the
+    softmax of the selected logits.  With a = W1_e x, b = W3_e x, s = SiLU(a),
+    h = s * b, o = W2_e h and y = sum_k g_k o_k:
+      d o_k = g_k dy,          d g_k = <dy, o_k>,
+      d h = W2_e^T d o,        d W2_e += d o h^T,
+      d a = d h * b * SiLU'(a), d b = d h * s,
+      d W1_e += d a x^T,       d W3_e += d b x^T,  d x += W1_e^T d a + W3_e^T d b,
+      d l_k = g_k (d g_k - sum_j g_j d g_j)  (softmax over the selected logits),
+      d W_g += x d l^T,        d x += W_g d l.
+    Returns dict(dx [T, dim], dwg [dim, n], dw1, dw3 [n, hidden, dim],
+    dw2 [n, dim, hidden]), float64.
+    """
+    xf, wg = _f64(x), _f64(w_gate)
+    W1, W3, W2 = _f64(w1), _f64(w3), _f64(w2)
+    g_up = _f64(dy)
+    ids, gates, _ = router(xf, wg, top_k)
+    T, dim = xf.shape
+    n = W1.shape[0]
+    dx = np.zeros_like(xf)
+    dwg = np.zeros_like(wg)
+    dw1, dw3, dw2 = np.zeros_like(W1), np.zeros_like(W3), np.zeros_like(W2)
+    dgate = np.zeros((T, top_k))
+    for e in range(n):
+        tok, slot = np.nonzero(ids == e)
+        if len(tok) == 0:
+            continue
+        xe = xf[tok]
+        a = xe @ W1[e].T
+        b = xe @ W3[e].T
+        s = silu(a)
+        h = s * b
+        o = h @ W2[e].T
+        do = gates[tok, slot][:, None] * g_up[tok]
+        dgate[tok, slot] = np.sum(g_up[tok] * o, axis=1)
+        dh = do @ W2[e]
+        dw2[e] += do.T @ h
+        da = dh * b * silu_grad(a)
+        db = dh * s
+        dw1[e] += da.T @ xe
+        dw3[e] += db.T @ xe
+        np.add.at(dx, tok, da @ W1[e] + db @ W3[e])
+    dl_sel = gates * (dgate - np.sum(gates * dgate, axis=1, keepdims=True))
+    dl = np.zeros((T, n))
+    np.put_along_axis(dl, ids, dl_sel, axis=1)
+    dwg += xf.T @ dl
+    dx += dl @ wg.T
+    return dict(dx=dx, dwg=dwg, dw1=dw1, dw3=dw3, dw2=dw2)
+
+
 def rmsnorm_bf16(x, eps: float) -> np.ndarray:
     """bf16 bits of x / sqrt(mean(x^2) + eps) per row (unit gain; stack workload only)."""
     xf = _f64(x)

@@ -132,3 +132,10 @@ def test_fine_grained_layer_160_experts_top8(path):
 def test_fine_grained_layer_full_dims_sampled():
     cfg = mi.CONFIGS["fine"].replace(T=1024)
     check_layer(cfg, 0, sample=32)
+
+
+@pytest.mark.parametrize("path", [0, 3])
+def test_mixtral_8x22b_dims(path):
+    # "Mixtral 8x22B, scaling the exact same architecture up": dim 6144, hidden 16384
+    cfg = mi.Config("8x22b", T=48, dim=6144, hidden=16384, seed=46108)
+    check_layer(cfg, path)

@@ -337,3 +337,70 @@ def test_stack_layer_residual_and_zero_experts():
     out, _, _, u = orc.stack_layer(xb, wg, W1, W3, W2, 2, 1e-5)
     want = orc.widen_bf16(xb) + orc.expert_ffn(orc.widen_bf16(u), w1[0], w3[0], w2[0])
     assert np.max(np.abs(out - want)) < 1e-12
+
+
+# ---------------------------------------------------------- backward -----
+
+def _loss(x, wg, w1, w3, w2, K, dy):
+    y, _, _ = orc.moe_layer(x, wg, w1, w3, w2, K)
+    return float(np.sum(y * dy))
+
+
+@pytest.mark.parametrize("n,K", [(8, 2), (4, 1), (5, 3)])
+def test_backward_matches_central_differences(n, K):
+    """Every gradient of the oracle's backward against central finite differences
+    of the forward (routing fixed: inputs whose top-K margin exceeds the step)."""
+    rng = np.random.default_rng(60 + n + K)
+    T, d, h = 5, 6, 7
+    x, wg, w1, w3, w2 = (rng.standard_normal(s) for s in
+                         [(T, d), (d, n), (n, h, d), (n, h, d), (n, d, h)])
+    dy = rng.standard_normal((T, d))
+    srt = -np.sort(-orc.router_logits(x, wg), axis=1)
+    if K < n:
+        assert np.min(srt[:, K - 1] - srt[:, K]) > 1e-3   # routing stays fixed under the step
+    g = orc.moe_layer_backward(x, wg, w1, w3, w2, K, dy)
+    eps = 1e-6
+    for name, arr in [("dx", x), ("dwg", wg), ("dw1", w1), ("dw3", w3), ("dw2", w2)]:
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss(x, wg, w1, w3, w2, K, dy)
+            arr[idx] = old - eps
+            lm = _loss(x, wg, w1, w3, w2, K, dy)
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.max(np.abs(num - g[name])) < 1e-6 * (1 + np.max(np.abs(num))), name
+
+
+def test_backward_single_expert_is_the_dense_swiglu_gradient():
+    """n = 1, K = 1: the gate is 1 and constant, so dW_g = 0 and every other
+    gradient is the plain SwiGLU FFN's (written here with the chain rule on
+    explicit per-element loops)."""
+    rng = np.random.default_rng(70)
+    T, d, h = 3, 4, 5
+    x = rng.standard_normal((T, d))
+    wg = rng.standard_normal((d, 1))
+    w1, w3 = rng.standard_normal((1, h, d)), rng.standard_normal((1, h, d))
+    w2 = rng.standard_normal((1, d, h))
+    dy = rng.standard_normal((T, d))
+    g = orc.moe_layer_backward(x, wg, w1, w3, w2, 1, dy)
+    assert np.all(g["dwg"] == 0)
+    dx = np.zeros((T, d))
+    dw2 = np.zeros((d, h))
+    for t in range(T):
+        a = [sum(w1[0, j, i] * x[t, i] for i in range(d)) for j in range(h)]
+        b = [sum(w3[0, j, i] * x[t, i] for i in range(d)) for j in range(h)]
+        sig = [1 / (1 + math.exp(-v)) for v in a]
+        hh = [a[j] * sig[j] * b[j] for j in range(h)]
+        dh = [sum(dy[t, i] * w2[0, i, j] for i in range(d)) for j in range(h)]
+        for i in range(d):
+            for j in range(h):
+                dw2[i, j] += dy[t, i] * hh[j]
+        for j in range(h):
+            da = dh[j] * b[j] * sig[j] * (1 + a[j] * (1 - sig[j]))
+            db = dh[j] * a[j] * sig[j]
+            for i in range(d):
+                dx[t, i] += da * w1[0, j, i] + db * w3[0, j, i]
+    assert np.max(np.abs(dx - g["dx"])) < 1e-12
+    assert np.max(np.abs(dw2 - g["dw2"][0])) < 1e-12
