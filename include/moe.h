@@ -159,6 +159,26 @@ MOE_API moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opt
                              float* gates, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* Backward pass of the layer (the gradient of section 2.1's
+ * y = sum_k G(x)_k E_k(x) for an upstream gradient dy, with the routing held
+ * fixed: TopK is piecewise constant, so W_g and x receive the gradient of the
+ * softmax over the selected logits).  Recomputes the forward (router,
+ * grouping, expert FFN keeping the gate/up pre-activations) in `ws`, then:
+ *   dx [T, dim] bf16;  dw_gate [dim, n], dw1 / dw3 [n, hidden, dim],
+ *   dw2 [n, dim, hidden] float32 (overwritten, not accumulated).
+ * The expert-weight gradients are summed over the tokens routed to each
+ * expert by tcgen05 GEMMs; every sum has a fixed order (deterministic).
+ * Needs dim and hidden multiples of 256 (MOE_ERR_UNSUPPORTED_SHAPE otherwise)
+ * and a workspace of moe_backward_workspace_bytes(shape) bytes, initialised
+ * with moe_workspace_init.  No RMSNorm / residual option. */
+MOE_API size_t moe_backward_workspace_bytes(const moe_shape* shape);
+MOE_API moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x,
+                                      const moe_bf16* w_gate, const moe_bf16* w1,
+                                      const moe_bf16* w3, const moe_bf16* w2,
+                                      const moe_bf16* dy, moe_bf16* dx, float* dw_gate,
+                                      float* dw1, float* dw3, float* dw2, void* ws,
+                                      size_t ws_bytes, void* stream);
+
 /* Routing statistics ("Mixtral of Experts" section 5, Routing analysis) of
  * the expert ids [T, K] produced by moe_router_topk or moe_layer_forward:
  *   slot_counts [K * n]  slot_counts[k*n + e] = tokens whose k-th choice is

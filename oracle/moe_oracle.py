@@ -170,7 +170,7 @@ def silu_grad(a: np.ndarray) -> np.ndarray:
     return sg * (1.0 + a * (1.0 - sg))
 
 
-def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy):
+def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool = False):
     """Gradients of the sparse MoE layer (§2.1) for an upstream gradient dy.
 
     The routing (which K experts each token uses) is held fixed: TopK is
@@ -185,7 +185,14 @@ def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy):
       d W_g += x d l^T,        d x += W_g d l.
     Returns dict(dx [T, dim], dwg [dim, n], dw1, dw3 [n, hidden, dim],
     dw2 [n, dim, hidden]), float64.
+
+    bf16_points: round to bf16 where a bf16 pipeline stores intermediates (h,
+    formed from the unrounded pre-activations; the pre-activations a and b
+    kept for the backward; the expert outputs o, g_k dy, da and db, and each
+    expert's input-gradient rows), everything else in fp64; the exact mode
+    (default) rounds nothing.
     """
+    rnd = (lambda v: widen_bf16(round_bf16(v))) if bf16_points else (lambda v: v)
     xf, wg = _f64(x), _f64(w_gate)
     W1, W3, W2 = _f64(w1), _f64(w3), _f64(w2)
     g_up = _f64(dy)
@@ -201,20 +208,21 @@ def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy):
         if len(tok) == 0:
             continue
         xe = xf[tok]
-        a = xe @ W1[e].T
-        b = xe @ W3[e].T
+        a_x = xe @ W1[e].T
+        b_x = xe @ W3[e].T
+        h = rnd(silu(a_x) * b_x)          # h from the unrounded pre-activations
+        a, b = rnd(a_x), rnd(b_x)         # the stored pre-activations feed the backward
         s = silu(a)
-        h = s * b
-        o = h @ W2[e].T
-        do = gates[tok, slot][:, None] * g_up[tok]
+        o = rnd(h @ W2[e].T)
+        do = rnd(gates[tok, slot][:, None] * g_up[tok])
         dgate[tok, slot] = np.sum(g_up[tok] * o, axis=1)
         dh = do @ W2[e]
         dw2[e] += do.T @ h
-        da = dh * b * silu_grad(a)
-        db = dh * s
+        da = rnd(dh * b * silu_grad(a))
+        db = rnd(dh * s)
         dw1[e] += da.T @ xe
         dw3[e] += db.T @ xe
-        np.add.at(dx, tok, da @ W1[e] + db @ W3[e])
+        np.add.at(dx, tok, rnd(da @ W1[e] + db @ W3[e]))
     dl_sel = gates * (dgate - np.sum(gates * dgate, axis=1, keepdims=True))
     dl = np.zeros((T, n))
     np.put_along_axis(dl, ids, dl_sel, axis=1)

@@ -14,7 +14,8 @@ from ._lib import (  # noqa: F401
     MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE_TOO_SMALL, MOE_FFN_AUTO, MOE_FFN_GROUPED_GEMM,
     MOE_FFN_PAIR_GEMM, MOE_FFN_WEIGHT_STREAM, MOE_OK, MoeError, MoeShape, make_shape, moe_check_error,
     moe_combine, moe_expert_ffn_grouped, moe_layer_forward, moe_permute, moe_permute_noalloc,
-    moe_router_topk, moe_routing_stats,
+    moe_router_topk, moe_routing_stats, moe_backward_workspace_bytes, moe_layer_backward,
+    new_backward_workspace,
     moe_selftest_wait_timeout, moe_workspace_bytes, moe_workspace_init, new_workspace)
 
 

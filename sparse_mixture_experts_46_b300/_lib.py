@@ -33,6 +33,7 @@ EXPORTS = (
     "moe_status_string", "moe_workspace_bytes", "moe_workspace_init", "moe_router_topk",
     "moe_permute", "moe_expert_ffn_grouped", "moe_combine", "moe_layer_forward",
     "moe_check_error", "moe_selftest_wait_timeout", "moe_permute_noalloc", "moe_routing_stats",
+    "moe_backward_workspace_bytes", "moe_layer_backward",
 )
 
 
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
         "moe_selftest_wait_timeout": (i32, [vp, sz, ctypes.c_uint64, vp]),
         "moe_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
         "moe_routing_stats": (i32, [sp, vp, vp, vp, vp]),
+        "moe_backward_workspace_bytes": (sz, [sp]),
+        "moe_layer_backward": (i32, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -191,6 +194,34 @@ def moe_combine(shape, y_perm, slot_row, gates, y, residual=None, stream=None) -
                             _ptr(slot_row, _I32, "slot_row"), _ptr(gates, _F32, "gates"),
                             _ptr(residual, _BF16, "residual", nullable=True),
                             _ptr(y, _BF16, "y"), _stream(stream)), "moe_combine")
+
+
+def moe_backward_workspace_bytes(shape) -> int:
+    s = _shape(shape)
+    n = _LIB.moe_backward_workspace_bytes(ctypes.byref(s))
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_backward_workspace_bytes")
+    return int(n)
+
+
+def new_backward_workspace(shape, device=None, stream=None) -> torch.Tensor:
+    """Allocate (through torch) and initialise a workspace for moe_layer_backward."""
+    ws = torch.empty(moe_backward_workspace_bytes(shape), dtype=torch.uint8,
+                     device=device or torch.device("cuda"))
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, dx, dw_gate, dw1, dw3, dw2, ws,
+                       stream=None) -> None:
+    s = _shape(shape)
+    _check(_LIB.moe_layer_backward(
+        ctypes.byref(s), _ptr(x, _BF16, "x"), _ptr(w_gate, _BF16, "w_gate"),
+        _ptr(w1, _BF16, "w1"), _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
+        _ptr(dy, _BF16, "dy"), _ptr(dx, _BF16, "dx"), _ptr(dw_gate, _F32, "dw_gate"),
+        _ptr(dw1, _F32, "dw1"), _ptr(dw3, _F32, "dw3"), _ptr(dw2, _F32, "dw2"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "moe_layer_backward")
 
 
 def moe_routing_stats(shape, ids, slot_counts, repeats, stream=None) -> None:

@@ -158,6 +158,21 @@ __device__ __forceinline__ int find_expert(const int* s_start, int n, int t) {
   return lo;
 }
 
+// Bounded wait that ignores the abort flag: lets copies and MMAs that are
+// already in flight land before a CTA exits (records kErrTimeoutDrain).
+__device__ __forceinline__ void pair_drain_wait_shared(uint64_t* bar, uint32_t parity,
+                                                       uint32_t* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrTimeoutDrain);
+      return;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- TMA ---
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {

@@ -68,6 +68,64 @@ WsLayout ws_layout(const moe_shape* s) {
   return L;
 }
 
+// Workspace of moe_layer_backward: the recomputed forward (with the gate/up
+// pre-activations), the activation gradients, the transposed operands of the
+// weight-gradient GEMMs and the transposed weights.
+struct BwdLayout {
+  size_t err, ids, gates, offsets, chunk_hist, chunk_base, perm_src, slot_row, poff;
+  size_t x_perm, h, ab, y_perm, dO, dab, dx_perm, dg, dl, dl_perm;
+  size_t dOT, hT, dabT, xT, w2T, w13T;
+  size_t total;
+  int nchunks, rpad;
+};
+
+static BwdLayout bwd_layout(const moe_shape* s) {
+  BwdLayout L{};
+  const size_t T = (size_t)s->T, R = T * (size_t)s->top_k, n = (size_t)s->n_experts;
+  const size_t d = (size_t)s->dim, h = (size_t)s->hidden;
+  L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
+  L.rpad = (int)((R + 63 * n + 63) / 64 * 64);  // every expert's rows padded to 64
+  const size_t rp = (size_t)L.rpad;
+  size_t off = kWsControlBytes;
+  L.err = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L.ids = take(R * 4);
+  L.gates = take(R * 4);
+  L.offsets = take((n + 1) * 4);
+  L.chunk_hist = take((size_t)L.nchunks * n * 4);
+  L.chunk_base = take((size_t)L.nchunks * n * 4);
+  L.perm_src = take(R * 4);
+  L.slot_row = take(R * 4);
+  L.poff = take((n + 1) * 4);
+  L.x_perm = take(R * d * 2);
+  L.h = take(R * h * 2);
+  L.ab = take(R * 2 * h * 2);
+  L.y_perm = take(R * d * 2);
+  L.dO = take(R * d * 2);
+  L.dab = take(R * 2 * h * 2);
+  L.dx_perm = take(R * d * 2);
+  L.dg = take(R * 4);
+  L.dl = take(R * 4);
+  L.dl_perm = take(R * 4);
+  L.dOT = take(d * rp * 2);
+  L.hT = take(h * rp * 2);
+  L.dabT = take(2 * h * rp * 2);
+  L.xT = take(d * rp * 2);
+  L.w2T = take(n * h * d * 2);
+  L.w13T = take(n * d * 2 * h * 2);
+  L.total = off;
+  return L;
+}
+
+static bool backward_supported(const moe_shape* s) {
+  return shape_supported(s) && s->dim % 256 == 0 && s->hidden % 256 == 0 &&
+         (int64_t)s->T * s->top_k * 2 * s->hidden < (int64_t(1) << 31);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -233,6 +291,98 @@ moe_status moe_routing_stats(const moe_shape* shape, const int32_t* ids, int32_t
   if (shape->T > 0 && !ok_ptr(ids)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_routing_stats(*shape, ids, slot_counts, repeats,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_backward_workspace_bytes(const moe_shape* shape) {
+  if (!backward_supported(shape)) return 0;
+  return bwd_layout(shape).total;
+}
+
+moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* w_gate,
+                              const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
+                              const moe_bf16* dy, moe_bf16* dx, float* dw_gate, float* dw1,
+                              float* dw3, float* dw2, void* ws, size_t ws_bytes, void* stream) {
+  if (shape == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!backward_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ok_ptr(ws) || !ok_ptr(w_gate) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) ||
+      !ok_ptr(dw_gate) || !ok_ptr(dw1) || !ok_ptr(dw3) || !ok_ptr(dw2))
+    return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!ok_ptr(x) || !ok_ptr(dy) || !ok_ptr(dx))) return MOE_ERR_INVALID_ARG;
+  const BwdLayout L = bwd_layout(shape);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const moe_shape& s = *shape;
+  const int T = s.T, K = s.top_k, n = s.n_experts, d = s.dim, h = s.hidden, R = T * K;
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  const int64_t nw = (int64_t)n * h * d;  // elements of one expert-weight tensor
+  if (T == 0) {
+    // no tokens: every weight gradient is zero
+    cudaError_t e = cudaMemsetAsync(dw_gate, 0, sizeof(float) * (size_t)d * n, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw1, 0, sizeof(float) * (size_t)nw, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw3, 0, sizeof(float) * (size_t)nw, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, sizeof(float) * (size_t)nw, st);
+    return cuda_status(e);
+  }
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* gates = at<float>(ws, L.gates);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+  int32_t* poff = at<int32_t>(ws, L.poff);
+  uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
+  uint16_t* hb = at<uint16_t>(ws, L.h);
+  uint16_t* ab = at<uint16_t>(ws, L.ab);
+  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+  uint16_t* dO = at<uint16_t>(ws, L.dO);
+  uint16_t* dab = at<uint16_t>(ws, L.dab);
+  uint16_t* dx_perm = at<uint16_t>(ws, L.dx_perm);
+  float* dg = at<float>(ws, L.dg);
+  float* dl = at<float>(ws, L.dl);
+  float* dl_perm = at<float>(ws, L.dl_perm);
+  uint16_t* w2T = at<uint16_t>(ws, L.w2T);
+  uint16_t* w13T = at<uint16_t>(ws, L.w13T);
+  uint16_t* dOT = at<uint16_t>(ws, L.dOT);
+  uint16_t* hT = at<uint16_t>(ws, L.hT);
+  uint16_t* dabT = at<uint16_t>(ws, L.dabT);
+  uint16_t* xT = at<uint16_t>(ws, L.xT);
+
+#define MOE_TRY(call)                           \
+  do {                                          \
+    const cudaError_t e_ = (call);              \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+  // forward, recomputed: routing, grouping, expert FFN keeping the pre-activations
+  MOE_TRY(launch_router(s, x, w_gate, ids, gates, nullptr, nullptr, 0.0f, err, st));
+  MOE_TRY(launch_permute(s, x, ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
+                         at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src), slot_row,
+                         x_perm, L.nchunks, st));
+  MOE_TRY(launch_expert_ffn_pair(s, x_perm, offsets, w1, w3, w2, hb, y_perm, err, st, ab));
+  // gated combine and router
+  MOE_TRY(launch_combine_bwd(s, dy, y_perm, slot_row, gates, dO, dg, st));
+  MOE_TRY(launch_router_bwd(s, gates, dg, slot_row, dl, dl_perm, st));
+  MOE_TRY(launch_router_wgrad(s, x_perm, dl_perm, offsets, dw_gate, st));
+  // expert weights in the layouts of the activation-gradient GEMMs:
+  // W2T[e] = W2[e]^T [h, d];  W13T[e] = [W1[e]^T | W3[e]^T] [d, 2h]
+  MOE_TRY(launch_transpose_batched(w2, n, d, h, h, (int64_t)d * h, w2T, d, 0, (int64_t)h * d, st));
+  MOE_TRY(launch_transpose_batched(w1, n, h, d, d, (int64_t)h * d, w13T, 2 * h, 0,
+                                   (int64_t)d * 2 * h, st));
+  MOE_TRY(launch_transpose_batched(w3, n, h, d, d, (int64_t)h * d, w13T, 2 * h, h,
+                                   (int64_t)d * 2 * h, st));
+  // dH = dO W2 -> [dA | dG] (SwiGLU backward from the saved pre-activations)
+  MOE_TRY(launch_pair_rowgemm(dO, offsets, R, n, h, d, w2T, dab, 2 * h, ab, err, st));
+  // dX_perm = dA W1 + dG W3
+  MOE_TRY(launch_pair_rowgemm(dab, offsets, R, n, d, 2 * h, w13T, dx_perm, d, nullptr, err, st));
+  MOE_TRY(launch_input_grad(s, dx_perm, slot_row, ids, dl, w_gate, dx, st));
+  // weight gradients over each expert's padded rows
+  MOE_TRY(launch_pad_offsets(offsets, n, R, poff, st));
+  MOE_TRY(launch_transpose_grouped(dO, d, d, offsets, poff, n, R, L.rpad, dOT, L.rpad, st));
+  MOE_TRY(launch_transpose_grouped(hb, h, h, offsets, poff, n, R, L.rpad, hT, L.rpad, st));
+  MOE_TRY(launch_transpose_grouped(dab, 2 * h, 2 * h, offsets, poff, n, R, L.rpad, dabT, L.rpad,
+                                   st));
+  MOE_TRY(launch_transpose_grouped(x_perm, d, d, offsets, poff, n, R, L.rpad, xT, L.rpad, st));
+  MOE_TRY(launch_wgrad(dOT, hT, d, h, L.rpad, poff, n, dw2, dw2, d, (int64_t)d * h, err, st));
+  MOE_TRY(launch_wgrad(dabT, xT, 2 * h, d, L.rpad, poff, n, dw1, dw3, h, (int64_t)h * d, err, st));
+#undef MOE_TRY
+  return MOE_OK;
 }
 
 moe_status moe_check_error(void* ws, void* stream) {

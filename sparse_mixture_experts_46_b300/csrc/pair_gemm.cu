@@ -46,6 +46,15 @@
 
 namespace moe {
 
+// Epilogue of a pass: what the accumulator (out[r][j] = sum_k act[r][k] W_e[j][k])
+// becomes.
+enum : int {
+  kEpiPlain = 0,      // out = bf16(acc)
+  kEpiGlu = 1,        // W1/W3 stacked: out = bf16(SiLU(a) * g)
+  kEpiGluSave = 2,    // as kEpiGlu, and save[r] = [bf16(a) | bf16(g)] (pre-activations)
+  kEpiSwigluBwd = 3,  // acc = dH; from saved a, g: out[r] = [dA | dG] (SwiGLU backward)
+};
+
 struct PairArgs {
   const int32_t* offsets;  // [n + 1] grouped-row offsets (device)
   uint16_t* out;           // H [R, hidden] (gate/up) or y_perm [R, dim] (down)
@@ -57,6 +66,8 @@ struct PairArgs {
   int w_rows_per_expert;   // rows of one expert's weight matrix (hidden or dim)
   int out_ld;              // output row stride in elements
   int rows_total;          // R: grouped rows (offsets are clamped to [0, R])
+  uint16_t* save;          // kEpiGluSave: [R, 2 * out_ld] pre-activations a | g
+  const uint16_t* saved;   // kEpiSwigluBwd: [R, out_ld] pre-activations a | g (out_ld = 2h)
 };
 
 template <bool GLU, int STAGES>
@@ -91,11 +102,12 @@ __device__ __forceinline__ void pair_drain_wait(uint64_t* bar, uint32_t parity, 
   }
 }
 
-template <bool GLU, int STAGES>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1, const PairArgs args) {
+  constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
   using C = PairCfg<GLU, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   // Both CTAs of the pair place every tile at the same shared-memory offset:
@@ -281,8 +293,15 @@ __global__ void __launch_bounds__(192, 1)
               uint2 o;
               o.x = pack_bf16x2(silu_mul(a.x, g.x), silu_mul(a.y, g.y));
               o.y = pack_bf16x2(silu_mul(a.z, g.z), silu_mul(a.w, g.w));
-              *reinterpret_cast<uint2*>(args.out + (size_t)(row0 + c0 + col) * args.out_ld +
-                                        col0 + jq * 4) = o;
+              const size_t row = (size_t)(row0 + c0 + col);
+              *reinterpret_cast<uint2*>(args.out + row * args.out_ld + col0 + jq * 4) = o;
+              if (EPI == kEpiGluSave) {
+                uint16_t* sv = args.save + row * 2 * args.out_ld + col0 + jq * 4;
+                *reinterpret_cast<uint2*>(sv) =
+                    make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+                *reinterpret_cast<uint2*>(sv + args.out_ld) =
+                    make_uint2(pack_bf16x2(g.x, g.y), pack_bf16x2(g.z, g.w));
+              }
             }
           }
         } else {
@@ -294,11 +313,37 @@ __global__ void __launch_bounds__(192, 1)
             const int jq = item & 31;
             if (c0 + col < rows) {
               const float4 a = *reinterpret_cast<const float4*>(staging + col * 128 + jq * 4);
-              uint2 o;
-              o.x = pack_bf16x2(a.x, a.y);
-              o.y = pack_bf16x2(a.z, a.w);
-              *reinterpret_cast<uint2*>(args.out + (size_t)(row0 + c0 + col) * args.out_ld +
-                                        col0 + jq * 4) = o;
+              const size_t row = (size_t)(row0 + c0 + col);
+              if (EPI == kEpiSwigluBwd) {
+                // a = dH; with the saved pre-activations z (gate) and g (up):
+                // dZ = dH * g * SiLU'(z), dG = dH * SiLU(z)
+                const int hh = args.out_ld / 2;
+                const uint2 zb = *reinterpret_cast<const uint2*>(args.saved + row * args.out_ld +
+                                                                 col0 + jq * 4);
+                const uint2 gb = *reinterpret_cast<const uint2*>(args.saved + row * args.out_ld +
+                                                                 hh + col0 + jq * 4);
+                const float dh[4] = {a.x, a.y, a.z, a.w};
+                const float z[4] = {__uint_as_float(zb.x << 16), __uint_as_float(zb.x & 0xFFFF0000u),
+                                    __uint_as_float(zb.y << 16), __uint_as_float(zb.y & 0xFFFF0000u)};
+                const float g[4] = {__uint_as_float(gb.x << 16), __uint_as_float(gb.x & 0xFFFF0000u),
+                                    __uint_as_float(gb.y << 16), __uint_as_float(gb.y & 0xFFFF0000u)};
+                float dz[4], dg[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float sg = 1.0f / (1.0f + __expf(-z[u]));
+                  dz[u] = dh[u] * g[u] * sg * (1.0f + z[u] * (1.0f - sg));
+                  dg[u] = dh[u] * z[u] * sg;
+                }
+                *reinterpret_cast<uint2*>(args.out + row * args.out_ld + col0 + jq * 4) =
+                    make_uint2(pack_bf16x2(dz[0], dz[1]), pack_bf16x2(dz[2], dz[3]));
+                *reinterpret_cast<uint2*>(args.out + row * args.out_ld + hh + col0 + jq * 4) =
+                    make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
+              } else {
+                uint2 o;
+                o.x = pack_bf16x2(a.x, a.y);
+                o.y = pack_bf16x2(a.z, a.w);
+                *reinterpret_cast<uint2*>(args.out + row * args.out_ld + col0 + jq * 4) = o;
+              }
             }
           }
         }
@@ -349,10 +394,11 @@ static bool pair_encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uin
 }
 
 // Grid of the pair kernel: two CTAs per co-resident cluster, at most one CTA per SM.
-template <bool GLU, int STAGES>
+template <int EPI, int STAGES>
 static int pair_grid(cudaError_t* err) {
+  constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
   using C = PairCfg<GLU, STAGES>;
-  auto kern = pair_gemm_kernel<GLU, STAGES>;
+  auto kern = pair_gemm_kernel<EPI, STAGES>;
   static int cached[64] = {0};
   int dev = 0;
   *err = cudaGetDevice(&dev);
@@ -385,12 +431,13 @@ static int pair_grid(cudaError_t* err) {
   return grid;
 }
 
-template <bool GLU, int STAGES>
+template <int EPI, int STAGES>
 static cudaError_t run_pair_gemm(const CUtensorMap& a, const CUtensorMap& w0,
                                  const CUtensorMap& w1, const PairArgs& args, cudaStream_t st) {
+  constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
   using C = PairCfg<GLU, STAGES>;
   cudaError_t e = cudaSuccess;
-  const int grid = pair_grid<GLU, STAGES>(&e);
+  const int grid = pair_grid<EPI, STAGES>(&e);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -406,7 +453,7 @@ static cudaError_t run_pair_gemm(const CUtensorMap& a, const CUtensorMap& w0,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<GLU, STAGES>, a, w0, w1, args);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<EPI, STAGES>, a, w0, w1, args);
 }
 
 bool pair_ffn_supported(const moe_shape& s) { return s.dim % 256 == 0 && s.hidden % 128 == 0; }
@@ -414,7 +461,7 @@ bool pair_ffn_supported(const moe_shape& s) { return s.dim % 256 == 0 && s.hidde
 cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
                                    const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
                                    const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
-                                   uint32_t* err, cudaStream_t st) {
+                                   uint32_t* err, cudaStream_t st, uint16_t* save) {
   const int R = s.T * s.top_k;
   if (R == 0) return cudaSuccess;
   if (!pair_ffn_supported(s)) return cudaErrorInvalidValue;
@@ -426,11 +473,32 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
       !pair_encode_2d(&tm_h, h, hd, R, 128) ||
       !pair_encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 128))
     return cudaErrorInvalidValue;
-  const PairArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R};
-  cudaError_t e = run_pair_gemm<true, 6>(tm_x, tm_w1, tm_w3, a1, st);
+  const PairArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R, save, nullptr};
+  cudaError_t e = save != nullptr ? run_pair_gemm<kEpiGluSave, 6>(tm_x, tm_w1, tm_w3, a1, st)
+                                  : run_pair_gemm<kEpiGlu, 6>(tm_x, tm_w1, tm_w3, a1, st);
   if (e != cudaSuccess) return e;
-  const PairArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 256, d, d, R};
-  return run_pair_gemm<false, 6>(tm_h, tm_w2, tm_w2, a2, st);
+  const PairArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 256, d, d, R, nullptr,
+                    nullptr};
+  return run_pair_gemm<kEpiPlain, 6>(tm_h, tm_w2, tm_w2, a2, st);
+}
+
+// out[r][j] = bf16(sum_k act[r][k] W[e][j][k]) over the grouped rows r of each
+// expert e: act [R, K], W [n, M, K] (M % 256 == 0, K % 64 == 0), out rows of
+// out_ld elements (columns j < M).  With `saved` ([R, 2M] pre-activations
+// a | g) the epilogue is the SwiGLU backward: the accumulator is dH and
+// out = [dA | dG] (out_ld = 2M).
+cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int R, int n, int M,
+                                int K, const uint16_t* w, uint16_t* out, int out_ld,
+                                const uint16_t* saved, uint32_t* err, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  if (M % 256 != 0 || K % 64 != 0) return cudaErrorInvalidValue;
+  CUtensorMap tm_a, tm_w;
+  if (!pair_encode_2d(&tm_a, act, K, R, 128) || !pair_encode_2d(&tm_w, w, K, (uint64_t)n * M, 128))
+    return cudaErrorInvalidValue;
+  const PairArgs a{offsets, out, err, kWaitLimitNs, n, K / 64, M / 256, M, out_ld, R, nullptr,
+                   saved};
+  if (saved != nullptr) return run_pair_gemm<kEpiSwigluBwd, 6>(tm_a, tm_w, tm_w, a, st);
+  return run_pair_gemm<kEpiPlain, 6>(tm_a, tm_w, tm_w, a, st);
 }
 
 }  // namespace moe

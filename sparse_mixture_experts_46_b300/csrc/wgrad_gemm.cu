@@ -1,0 +1,300 @@
+// wgrad_gemm.cu -- weight gradients of the expert SwiGLU FFN on CTA pairs
+// (tcgen05 cta_group::2): for every expert e
+//   C_e[m][n] = sum over the rows r of expert e of P[r][m] * Q[r][n]   (fp32)
+// ("Mixtral of Experts" section 2.1: dW2_e = dO_e^T H_e, dW1_e = dA_e^T X_e,
+// dW3_e = dG_e^T X_e, the expert weights' gradients summed over the tokens
+// routed to the expert).
+//
+// Both operands arrive transposed, [M, Rpad] and [N, Rpad], with each expert's
+// rows padded with zeros to a multiple of 64 (columns [poff[e], poff[e+1])),
+// so the reduction over an expert's tokens is a run of whole 64-wide K blocks
+// in the usual K-major, 128-byte-swizzled layout.  A pair owns a 256 x 256
+// output tile (each CTA 128 rows of P and half of the 256 rows of Q, the MMA
+// M = 256 spread over both); the accumulator (2 x 256 TMEM columns, double
+// buffered) is written out by each thread as its own fp32 output row segment.
+// Work units: (expert, 256-row block of M, 256-column block of N), round robin
+// over the pairs.  An expert without tokens writes zeros.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+struct WgradArgs {
+  const int32_t* poff;  // [n + 1] padded row offsets (multiples of 64)
+  float* out0;          // rows m < m_split: out0[e][m][n]
+  float* out1;          // rows m >= m_split: out1[e][m - m_split][n] (may equal out0)
+  int64_t out_estride;  // elements per expert in out0 / out1
+  int m_split;
+  int m_blocks;         // M / 256
+  int n_blocks;         // N / 256
+  int N;                // output row length
+  int n_experts;
+  uint32_t* err;
+  uint64_t limit_ns;
+};
+
+constexpr int kWgStages = 6;
+constexpr int kWgStageBytes = 2 * 128 * 128;  // 128 rows of P + 128 rows of Q (64 K each)
+constexpr int kWgSmemBytes = kWgStages * kWgStageBytes + 2048 + 1024;
+
+__global__ void __launch_bounds__(192, 1)
+    wgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_p,
+                      const __grid_constant__ CUtensorMap tm_q, const WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* aux = tiles + kWgStages * kWgStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty = full + kWgStages;
+  uint64_t* tfull = empty + kWgStages;  // [2]
+  uint64_t* tempty = tfull + 2;         // [2]
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_ok = abort_flag + 1;  // [2]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int per_expert = args.m_blocks * args.n_blocks;
+  const int total = args.n_experts * per_expert;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWgStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 2);
+    mbar_init(&tempty[1], 2);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_p);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
+
+  pdl_wait();  // the transposed operands and poff are written by earlier kernels
+  pdl_launch_dependents();
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
+  // unit -> expert, M block, N block, K blocks [kb0, kb0 + nkb)
+  auto decode = [&](int u, int& e, int& mb, int& nb, int& kb0, int& nkb) {
+    e = u / per_expert;
+    const int local = u - e * per_expert;
+    mb = local / args.n_blocks;
+    nb = local - mb * args.n_blocks;
+    kb0 = args.poff[e] >> 6;
+    nkb = (args.poff[e + 1] - args.poff[e]) >> 6;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < total; u += npairs) {
+        int e, mb, nb, kb0, nkb;
+        decode(u, e, mb, nb, kb0, nkb);
+        const int prow = mb * 256 + (int)rank * 128;
+        const int qrow = nb * 256 + (int)rank * 128;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kWgStages;
+          const uint32_t ph = (uint32_t)(it / kWgStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kWgStageBytes);
+          const uint32_t bar = smem_map_rank(smem_u32(&full[s]), 0);
+          uint8_t* st = tiles + s * kWgStageBytes;
+          const int kx = (kb0 + kb) * 64;
+          tma_load_2d_pair(st, &tm_p, kx, prow, bar);
+          tma_load_2d_pair(st + 128 * 128, &tm_q, kx, qrow, bar);
+        }
+      }
+      if (rank == 0)
+        for (int j = (it > kWgStages ? it - kWgStages : 0); j < it; ++j)
+          pair_drain_wait_shared(&full[j % kWgStages], (uint32_t)(j / kWgStages) & 1u, args.err,
+                                 args.limit_ns);
+    }
+  } else if (warp == 1) {
+    if (rank == 0 && lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16_f32(256, 256);
+      for (int u = pair; ok && u < total; u += npairs, ++lt) {
+        int e, mb, nb, kb0, nkb;
+        decode(u, e, mb, nb, kb0, nkb);
+        const int b = lt & 1;
+        const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + (uint32_t)(b * 256);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kWgStages;
+          const uint32_t ph = (uint32_t)(it / kWgStages) & 1u;
+          if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(tiles + s * kWgStageBytes);
+          const uint32_t sb = sa + 128 * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_pair(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
+                          idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit_pair_mc(&empty[s], 0x3);
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&tfull[b], 0x3);  // with no K block: arrives at once
+      }
+      mma_commit_pair_mc(drain, 0x1);
+      pair_drain_wait_shared(drain, 0, args.err, args.limit_ns);
+    }
+  } else {
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;
+    int lt = 0;
+    for (int u = pair; u < total; u += npairs, ++lt) {
+      const int b = lt & 1;
+      const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+      if (et == 0) s_ok[b] = mbar_wait(&tfull[b], tph, wctl, kErrTimeoutEpilogue) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!s_ok[b]) break;
+      tc_fence_after_sync();
+      int e, mb, nb, kb0, nkb;
+      decode(u, e, mb, nb, kb0, nkb);
+      const int m = mb * 256 + (int)rank * 128 + q * 32 + lane;  // this thread's output row
+      float* orow = m < args.m_split
+                        ? args.out0 + (int64_t)e * args.out_estride + (int64_t)m * args.N
+                        : args.out1 + (int64_t)e * args.out_estride +
+                              (int64_t)(m - args.m_split) * args.N;
+      float4* dst = reinterpret_cast<float4*>(orow + nb * 256);
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        float v[32];
+        if (nkb > 0) {
+          tmem_ld_32(tacc + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) dst[(c0 + i) / 4] = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+      tc_fence_before_sync();
+      named_bar_sync(1, 128);
+      if (et == 0) mbar_arrive_cluster(smem_map_rank(smem_u32(&tempty[b]), 0));
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host ---
+
+static PFN_cuTensorMapEncodeTiled_v12000 wg_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+static bool wg_encode(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows) {
+  auto enc = wg_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// C_e = P_e^T Q_e for every expert: pT [M, rpad_ld], qT [N, rpad_ld] (bf16,
+// expert e at columns [poff[e], poff[e+1])), M and N multiples of 256.
+cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, int rpad_ld,
+                         const int32_t* poff, int n, float* out0, float* out1, int m_split,
+                         int64_t out_estride, uint32_t* err, cudaStream_t st) {
+  if (M % 256 != 0 || N % 256 != 0 || rpad_ld % 64 != 0) return cudaErrorInvalidValue;
+  CUtensorMap tm_p, tm_q;
+  if (!wg_encode(&tm_p, pT, rpad_ld, M) || !wg_encode(&tm_q, qT, rpad_ld, N))
+    return cudaErrorInvalidValue;
+  static int grids[64] = {0};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int& grid = grids[dev];
+  if (grid == 0) {
+    cudaError_t e = cudaFuncSetAttribute(wgrad_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kWgSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = kWgSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, wgrad_pair_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    grid = 2 * clusters < (num_sms() & ~1) ? 2 * clusters : (num_sms() & ~1);
+  }
+  const WgradArgs a{poff, out0, out1, out_estride, m_split, M / 256, N / 256, N, n, err,
+                    kWaitLimitNs};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = kWgSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, wgrad_pair_kernel, tm_p, tm_q, a);
+}
+
+}  // namespace moe

@@ -1,0 +1,111 @@
+"""GPU layer backward (moe_layer_backward) against the oracle's fp64 gradients
+(which are pinned by central finite differences on the CPU), two ways:
+
+* exact oracle, per element |gpu - ref| <= 2e-2 |ref| + 8e-2 rms(ref): the
+  GPU stores the pre-activations, h, the expert outputs, g dy, dA / dG and
+  each expert's input-gradient rows in bf16 (each rounding at most 2^-9
+  relative), and a weight-gradient element that is a sum of a few tokens'
+  terms inherits one token's rounding error in full: replaying those
+  roundings in fp64 on the CPU for the 96-token case gives a largest error of
+  4.9 % of the gradient's RMS, on elements much smaller than the RMS;
+* oracle with the same bf16 rounding points, per element
+  |gpu - ref| <= 1e-2 |ref| + 3e-2 rms(ref): what is left is fp32
+  accumulation order and the odd value that rounds the other way -- one
+  bf16 ulp (2^-8 of it) of a per-expert input-gradient row that the sum
+  over the K experts then cancels down (a row element near 2 contributes
+  0.008 to a dx element near 0.01 in the 96-token case).
+A missing term does not fit inside either bound: the router's share of dx
+alone is ~36 % of dx's RMS here."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as orc
+from tests.gpu_util import dev_bf16, host_bits, lib
+from tests.inputs_filtered import filter_x
+
+pytestmark = pytest.mark.gpu
+
+EXACT = (2e-2, 8e-2)     # (rtol, atol as a fraction of the tensor's RMS)
+MATCHED = (1e-2, 3e-2)
+
+
+def close(name, got, ref, tol):
+    RTOL, ATOL_RMS = tol
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    scale = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    bound = RTOL * np.abs(ref) + ATOL_RMS * scale
+    err = np.abs(got - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError("%s: %d/%d out of tolerance (max err %.3g, rms %.3g); first %s: gpu %s ref %s"
+                             % (name, int(bad.sum()), bad.size, float(np.nanmax(err)), scale,
+                                idx.tolist(), [float(got[tuple(i)]) for i in idx],
+                                [float(ref[tuple(i)]) for i in idx]))
+
+
+def run_backward(cfg, L, dy):
+    moe = lib()
+    n, d, h = cfg.n_experts, cfg.dim, cfg.hidden
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dx = torch.full((max(cfg.T, 1), d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dwg = torch.full((d, n), float("nan"), **f32)
+    dw1 = torch.full((n, h, d), float("nan"), **f32)
+    dw3 = torch.full((n, h, d), float("nan"), **f32)
+    dw2 = torch.full((n, d, h), float("nan"), **f32)
+    ws = moe.new_backward_workspace(cfg)
+    if cfg.T > 0:
+        x, dyd = dev_bf16(L.x), dev_bf16(dy)
+    else:
+        x = dyd = torch.zeros((1, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_layer_backward(cfg, x, dev_bf16(L.wg), dev_bf16(L.w1), dev_bf16(L.w3),
+                           dev_bf16(L.w2), dyd, dx, dwg, dw1, dw3, dw2, ws)
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    return dict(dx=orc.widen_bf16(host_bits(dx[:cfg.T])), dwg=dwg.cpu().numpy(),
+                dw1=dw1.cpu().numpy(), dw3=dw3.cpu().numpy(), dw2=dw2.cpu().numpy())
+
+
+def check_backward(cfg):
+    L = mi.make_layer(cfg)
+    filter_x(cfg, L.x, L.wg, L.shift)
+    dy = mi.gen_x(cfg.replace(seed=cfg.seed + 1))
+    got = run_backward(cfg, L, dy)
+    ref = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy)
+    matched = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy, bf16_points=True)
+    for name in ("dx", "dwg", "dw1", "dw3", "dw2"):
+        close(name, got[name], ref[name], EXACT)
+        close(name + " (bf16 points)", got[name], matched[name], MATCHED)
+
+
+@pytest.mark.parametrize("T,n,K", [(96, 8, 2), (200, 8, 1), (150, 16, 2), (64, 40, 4), (7, 8, 2)])
+def test_backward_matches_oracle(T, n, K):
+    cfg = mi.Config("bwd", T=T, dim=256, hidden=256, n_experts=n, top_k=K, seed=46200 + T + n)
+    check_backward(cfg)
+
+
+def test_backward_wider_dims_and_ragged_groups():
+    # dim 512, hidden 768: several 256-wide tiles per expert in every GEMM
+    cfg = mi.Config("bwd", T=333, dim=512, hidden=768, seed=46300)
+    check_backward(cfg)
+
+
+def test_backward_zero_tokens_gives_zero_weight_gradients():
+    cfg = mi.Config("bwd", T=0, dim=256, hidden=256, seed=46301)
+    L = mi.make_layer(cfg)
+    got = run_backward(cfg, L, np.zeros((0, cfg.dim), np.uint16))
+    for name in ("dwg", "dw1", "dw3", "dw2"):
+        assert np.all(got[name] == 0), name
+
+
+def test_backward_is_deterministic():
+    cfg = mi.Config("bwd", T=120, dim=256, hidden=256, seed=46302)
+    L = mi.make_layer(cfg)
+    dy = mi.gen_x(cfg.replace(seed=46303))
+    a = run_backward(cfg, L, dy)
+    b = run_backward(cfg, L, dy)
+    for name in a:
+        assert np.array_equal(a[name], b[name]), name

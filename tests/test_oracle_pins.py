@@ -404,3 +404,17 @@ def test_backward_single_expert_is_the_dense_swiglu_gradient():
                 dx[t, i] += da * w1[0, j, i] + db * w3[0, j, i]
     assert np.max(np.abs(dx - g["dx"])) < 1e-12
     assert np.max(np.abs(dw2 - g["dw2"][0])) < 1e-12
+
+
+def test_backward_bf16_points_mode_stays_near_exact():
+    """The rounding-matched backward differs from the exact one by bf16-sized
+    errors only (and equals it when nothing needs rounding)."""
+    rng = np.random.default_rng(71)
+    x, wg, w1, w3, w2 = _rand_layer(rng, 40, 16, 24, 8)
+    dy = orc.widen_bf16(orc.round_bf16(rng.standard_normal((40, 16))))
+    a = orc.moe_layer_backward(x, wg, w1, w3, w2, 2, dy)
+    b = orc.moe_layer_backward(x, wg, w1, w3, w2, 2, dy, bf16_points=True)
+    for k in a:
+        rms = np.sqrt(np.mean(a[k] ** 2))
+        assert np.max(np.abs(a[k] - b[k])) < 0.1 * rms, k
+        assert np.max(np.abs(a[k] - b[k])) > 0, k
