@@ -15,6 +15,8 @@ reported beside it, as is the fp64 oracle timed on the host cores.
 
 --workload fine times the same step on the fine-grained variant the pages
 mention (top 8 of 160 smaller experts, expert hidden 1792) instead of Mixtral.
+--workload backward times moe_layer_backward (forward recompute + all
+gradients) on the Mixtral prefill batch (T=4096).
 
 Under torchrun (N > 1) every rank runs an independent replica (the layer has
 no cross-GPU exchange here); timing is max over ranks.
@@ -52,7 +54,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["backward"], default="mixtral")
     p.add_argument("--profile", choices=[DECODE, PREFILL, "fine_decode", "fine"], default=None,
                    help="no timing: run W warm-up + K layer calls of one workload (for ncu)")
     return p.parse_args()
@@ -433,6 +435,73 @@ def ffn_roofline(pre, pk, pk_kind, traffic):
             "unit": "GB/s", "frac": t_hbm, "traffic": traffic, "peak_kind": pk_kind + " copy"}
 
 
+def run_backward_bench(args, rank, world):
+    """The layer backward on the prefill batch: one step = one moe_layer_backward
+    call (forward recompute, then dx, dW_g, dW1, dW3, dW2)."""
+    import torch
+    import sparse_mixture_experts_46_b300 as moe
+    cfg, L = load_layer(PREFILL)
+    T, d, h, n, K = cfg.T, cfg.dim, cfg.hidden, cfg.n_experts, cfg.top_k
+    x, wg, w1, w3, w2 = (to_dev(a) for a in (L.x, L.wg, L.w1, L.w3, L.w2))
+    import moe_inputs as mi
+    dy = to_dev(mi.gen_x(cfg.replace(seed=cfg.seed + 1)))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dx = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    dwg = torch.empty((d, n), **f32)
+    dw1 = torch.empty((n, h, d), **f32)
+    dw3 = torch.empty((n, h, d), **f32)
+    dw2 = torch.empty((n, d, h), **f32)
+    ws = moe.new_backward_workspace(cfg)
+
+    def step():
+        moe.moe_layer_backward(cfg, x, wg, w1, w3, w2, dy, dx, dwg, dw1, dw3, dw2, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if moe.moe_check_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device error word after warm-up")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler()
+    barrier(world)
+    torch.cuda.synchronize()
+    import datetime
+    w0 = datetime.datetime.now()
+    start.record()
+    for _ in range(args.steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    w1t = datetime.datetime.now()
+    barrier(world)
+    clocks.mark(w0, w1t)
+    clk = clocks.stop()
+    ms = max_over_ranks(start.elapsed_time(end), world) / args.steps
+    R = T * K
+    flops = 18.0 * R * d * h + 2 * T * d * n * 3   # forward (6Rdh) + backward GEMMs (12Rdh) + router
+    pk, pk_kind = peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    result = {
+        "metric": "MoE-layer backward tokens/s at Mixtral dims (T=4096) + % of TC roofline",
+        "value": job_tokens_per_s(T, world, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator, Table 1 shapes, random-init weights)",
+        "config": {"workload": "Mixtral-shaped MoE layer backward (forward recompute + dx, dW_g, "
+                               "dW1, dW3, dW2), T=4096, dim 4096, hidden 14336, 8 experts, top-2",
+                   "T": T, "dim": d, "hidden": h, "n_experts": n, "top_k": K,
+                   "parallelism": "replicas"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
+                     "traffic": None, "peak_kind": pk_kind + " sustained bf16",
+                     "algorithmic_flop_per_step": flops},
+        "gpu_launches": args.steps * 21,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
 def main():
     args = parse()
     rank, world = dist_setup(args.gpus)
@@ -447,6 +516,12 @@ def main():
     import sparse_mixture_experts_46_b300 as moe
     if args.profile is not None:
         run_profile_case(args)
+        return
+    if args.workload == "backward":
+        run_backward_bench(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
     metric, dec_name, pre_name = WORKLOADS[args.workload]
     layers = {DECODE: load_layer(dec_name), PREFILL: load_layer(pre_name)}

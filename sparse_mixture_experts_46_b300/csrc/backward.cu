@@ -54,32 +54,6 @@ __global__ void __launch_bounds__(kMaxExperts) pad_offsets_kernel(const int32_t*
   if (e == 0) poff[n] = total;
 }
 
-// Batched transpose of bf16 matrices: dst[b][c][dcol0 + r] = src[b][r][c]
-// (src rows of src_ld elements, dst rows of dst_ld elements), 64 x 64 tiles
-// through shared memory.  Grid: (cols / 64, rows / 64, batches).
-__global__ void __launch_bounds__(256) transpose_batched_kernel(const uint16_t* __restrict__ src,
-                                                                int rows, int cols, int src_ld,
-                                                                int64_t src_bstride,
-                                                                uint16_t* __restrict__ dst,
-                                                                int dst_ld, int dcol0,
-                                                                int64_t dst_bstride) {
-  __shared__ uint16_t tile[64][66];
-  pdl_wait();
-  pdl_launch_dependents();
-  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
-  const uint16_t* s = src + (int64_t)blockIdx.z * src_bstride;
-  uint16_t* d = dst + (int64_t)blockIdx.z * dst_bstride;
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int r = i >> 6, c = i & 63;
-    tile[r][c] = (r0 + r < rows && c0 + c < cols) ? s[(int64_t)(r0 + r) * src_ld + c0 + c] : 0;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int c = i >> 6, r = i & 63;
-    if (c0 + c < cols && r0 + r < rows) d[(int64_t)(c0 + c) * dst_ld + dcol0 + r0 + r] = tile[r][c];
-  }
-}
-
 // Grouped activations [R, C] (expert e's rows at [offsets[e], offsets[e+1]))
 // -> dst [C, Rpad] with expert e's rows at columns [poff[e], poff[e] + count)
 // and zeros up to poff[e+1].  Grid: (C / 64, Rpad_max / 64).
@@ -242,14 +216,6 @@ static int cap_blocks(int64_t want) {
 cudaError_t launch_pad_offsets(const int32_t* offsets, int n, int R, int32_t* poff,
                                cudaStream_t st) {
   return launch_pdl(pad_offsets_kernel, dim3(1), dim3(kMaxExperts), 0, st, offsets, n, R, poff);
-}
-
-cudaError_t launch_transpose_batched(const uint16_t* src, int batches, int rows, int cols,
-                                     int src_ld, int64_t src_bstride, uint16_t* dst, int dst_ld,
-                                     int dcol0, int64_t dst_bstride, cudaStream_t st) {
-  const dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64), (unsigned)batches);
-  return launch_pdl(transpose_batched_kernel, grid, dim3(256), 0, st, src, rows, cols, src_ld,
-                    src_bstride, dst, dst_ld, dcol0, dst_bstride);
 }
 
 cudaError_t launch_transpose_grouped(const uint16_t* src, int C, int src_ld,

@@ -94,17 +94,17 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
                                    const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
                                    const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
                                    uint32_t* err, cudaStream_t st, uint16_t* save = nullptr);
-// out[r][j] = bf16(sum_k act[r][k] W[e][j][k]) per expert group (CTA-pair GEMM);
-// with `saved` ([R, M] pre-activations a | g) the SwiGLU backward: out = [dA | dG].
+// out[r][j] = bf16(sum_k act[r][k] B_e[k][j]) per expert group (CTA-pair GEMM),
+// B_e = rows of w0's expert block (then of w1's when K = 2 w_k_rows) in their
+// stored [k][j] layout; with `saved` ([R, 2M] pre-activations a | g) the SwiGLU
+// backward: out = [dA | dG].
 cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int R, int n, int M,
-                                int K, const uint16_t* w, uint16_t* out, int out_ld,
-                                const uint16_t* saved, uint32_t* err, cudaStream_t st);
+                                int K, const uint16_t* w0, const uint16_t* w1, int w_k_rows,
+                                uint16_t* out, int out_ld, const uint16_t* saved, uint32_t* err,
+                                cudaStream_t st);
 // Backward pass building blocks (backward.cu, wgrad_gemm.cu).
 cudaError_t launch_pad_offsets(const int32_t* offsets, int n, int R, int32_t* poff,
                                cudaStream_t st);
-cudaError_t launch_transpose_batched(const uint16_t* src, int batches, int rows, int cols,
-                                     int src_ld, int64_t src_bstride, uint16_t* dst, int dst_ld,
-                                     int dcol0, int64_t dst_bstride, cudaStream_t st);
 cudaError_t launch_transpose_grouped(const uint16_t* src, int C, int src_ld,
                                      const int32_t* offsets, const int32_t* poff, int n, int R,
                                      int rpad_max, uint16_t* dst, int dst_ld, cudaStream_t st);
@@ -121,7 +121,7 @@ cudaError_t launch_input_grad(const moe_shape& s, const uint16_t* dx_perm, const
                               cudaStream_t st);
 cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, int rpad_ld,
                          const int32_t* poff, int n, float* out0, float* out1, int m_split,
-                         int64_t out_estride, uint32_t* err, cudaStream_t st);
+                         uint32_t* err, cudaStream_t st);
 
 // Routing statistics (slot_counts [K * n], repeats [2]); zeroes both first.
 cudaError_t launch_routing_stats(const moe_shape& s, const int32_t* ids, int32_t* slot_counts,

@@ -69,12 +69,12 @@ WsLayout ws_layout(const moe_shape* s) {
 }
 
 // Workspace of moe_layer_backward: the recomputed forward (with the gate/up
-// pre-activations), the activation gradients, the transposed operands of the
-// weight-gradient GEMMs and the transposed weights.
+// pre-activations), the activation gradients and the transposed operands of
+// the weight-gradient GEMMs.
 struct BwdLayout {
   size_t err, ids, gates, offsets, chunk_hist, chunk_base, perm_src, slot_row, poff;
   size_t x_perm, h, ab, y_perm, dO, dab, dx_perm, dg, dl, dl_perm;
-  size_t dOT, hT, dabT, xT, w2T, w13T;
+  size_t dOT, hT, dabT, xT;
   size_t total;
   int nchunks, rpad;
 };
@@ -115,8 +115,6 @@ static BwdLayout bwd_layout(const moe_shape* s) {
   L.hT = take(h * rp * 2);
   L.dabT = take(2 * h * rp * 2);
   L.xT = take(d * rp * 2);
-  L.w2T = take(n * h * d * 2);
-  L.w13T = take(n * d * 2 * h * 2);
   L.total = off;
   return L;
 }
@@ -338,8 +336,6 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   float* dg = at<float>(ws, L.dg);
   float* dl = at<float>(ws, L.dl);
   float* dl_perm = at<float>(ws, L.dl_perm);
-  uint16_t* w2T = at<uint16_t>(ws, L.w2T);
-  uint16_t* w13T = at<uint16_t>(ws, L.w13T);
   uint16_t* dOT = at<uint16_t>(ws, L.dOT);
   uint16_t* hT = at<uint16_t>(ws, L.hT);
   uint16_t* dabT = at<uint16_t>(ws, L.dabT);
@@ -360,17 +356,12 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   MOE_TRY(launch_combine_bwd(s, dy, y_perm, slot_row, gates, dO, dg, st));
   MOE_TRY(launch_router_bwd(s, gates, dg, slot_row, dl, dl_perm, st));
   MOE_TRY(launch_router_wgrad(s, x_perm, dl_perm, offsets, dw_gate, st));
-  // expert weights in the layouts of the activation-gradient GEMMs:
-  // W2T[e] = W2[e]^T [h, d];  W13T[e] = [W1[e]^T | W3[e]^T] [d, 2h]
-  MOE_TRY(launch_transpose_batched(w2, n, d, h, h, (int64_t)d * h, w2T, d, 0, (int64_t)h * d, st));
-  MOE_TRY(launch_transpose_batched(w1, n, h, d, d, (int64_t)h * d, w13T, 2 * h, 0,
-                                   (int64_t)d * 2 * h, st));
-  MOE_TRY(launch_transpose_batched(w3, n, h, d, d, (int64_t)h * d, w13T, 2 * h, h,
-                                   (int64_t)d * 2 * h, st));
-  // dH = dO W2 -> [dA | dG] (SwiGLU backward from the saved pre-activations)
-  MOE_TRY(launch_pair_rowgemm(dO, offsets, R, n, h, d, w2T, dab, 2 * h, ab, err, st));
+  // dH = dO W2 -> [dA | dG] (SwiGLU backward from the saved pre-activations);
+  // the weights are read in their stored layout (reduction over their rows)
+  MOE_TRY(launch_pair_rowgemm(dO, offsets, R, n, h, d, w2, nullptr, d, dab, 2 * h, ab, err, st));
   // dX_perm = dA W1 + dG W3
-  MOE_TRY(launch_pair_rowgemm(dab, offsets, R, n, d, 2 * h, w13T, dx_perm, d, nullptr, err, st));
+  MOE_TRY(launch_pair_rowgemm(dab, offsets, R, n, d, 2 * h, w1, w3, h, dx_perm, d, nullptr, err,
+                              st));
   MOE_TRY(launch_input_grad(s, dx_perm, slot_row, ids, dl, w_gate, dx, st));
   // weight gradients over each expert's padded rows
   MOE_TRY(launch_pad_offsets(offsets, n, R, poff, st));
@@ -379,8 +370,8 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   MOE_TRY(launch_transpose_grouped(dab, 2 * h, 2 * h, offsets, poff, n, R, L.rpad, dabT, L.rpad,
                                    st));
   MOE_TRY(launch_transpose_grouped(x_perm, d, d, offsets, poff, n, R, L.rpad, xT, L.rpad, st));
-  MOE_TRY(launch_wgrad(dOT, hT, d, h, L.rpad, poff, n, dw2, dw2, d, (int64_t)d * h, err, st));
-  MOE_TRY(launch_wgrad(dabT, xT, 2 * h, d, L.rpad, poff, n, dw1, dw3, h, (int64_t)h * d, err, st));
+  MOE_TRY(launch_wgrad(dOT, hT, d, h, L.rpad, poff, n, dw2, dw2, d, err, st));
+  MOE_TRY(launch_wgrad(dabT, xT, 2 * h, d, L.rpad, poff, n, dw1, dw3, h, err, st));
 #undef MOE_TRY
   return MOE_OK;
 }

@@ -35,6 +35,13 @@
 // token tile) are scheduled from the device-resident offsets, expert-major,
 // then weight tile, then token tile, round-robin over the pairs.
 //
+// The same kernel serves the activation-gradient GEMMs of the backward pass
+// with the weights read in their stored layout (AMN): there the reduction
+// runs over the weight matrix's ROWS (dH = dO W2_e, dX = dA W1_e + dG W3_e),
+// so each CTA's A tile is taken as two boxes of 64 weight columns x 64 weight
+// rows -- the MN-major operand layout -- and marked MN-major in the
+// instruction descriptor; no transposed copy of any weight is made.
+//
 // Every wait is bounded (device.cuh); an expired wait records the error word
 // and the CTA winds down through the same exit path.
 #include <cudaTypedefs.h>
@@ -68,6 +75,10 @@ struct PairArgs {
   int rows_total;          // R: grouped rows (offsets are clamped to [0, R])
   uint16_t* save;          // kEpiGluSave: [R, 2 * out_ld] pre-activations a | g
   const uint16_t* saved;   // kEpiSwigluBwd: [R, out_ld] pre-activations a | g (out_ld = 2h)
+  // AMN only: the reduction walks w_k_rows rows of tm_w0's expert block for
+  // K blocks [0, k_split), then the same rows of tm_w1's for the rest
+  int k_split;
+  int w_k_rows;
 };
 
 template <bool GLU, int STAGES>
@@ -102,12 +113,13 @@ __device__ __forceinline__ void pair_drain_wait(uint64_t* bar, uint32_t parity, 
   }
 }
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool AMN>
 __global__ void __launch_bounds__(192, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1, const PairArgs args) {
   constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
+  static_assert(!(AMN && GLU), "stored-layout weights serve the plain and SwiGLU-backward passes");
   using C = PairCfg<GLU, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   // Both CTAs of the pair place every tile at the same shared-memory offset:
@@ -207,8 +219,18 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t bar = smem_map_rank(smem_u32(&full[s]), 0);
           uint8_t* st = tiles + s * C::STAGE_BYTES;
           const int kx = kb * C::BK;
-          tma_load_2d_pair(st, &tm_w0, kx, w_row, bar);
-          if (GLU) tma_load_2d_pair(st + C::A_BYTES / 2, &tm_w1, kx, w_row, bar);
+          if (AMN) {
+            // weight rows are the reduction: two 64-column boxes of 64 rows
+            const bool hi = kb >= args.k_split;
+            const CUtensorMap* tw = hi ? &tm_w1 : &tm_w0;
+            const int ky = e * args.w_k_rows + (hi ? kb - args.k_split : kb) * C::BK;
+            const int m0 = wt * 2 * C::W_ROWS + (int)rank * C::W_ROWS;
+            tma_load_2d_pair(st, tw, m0, ky, bar);
+            tma_load_2d_pair(st + C::A_BYTES / 2, tw, m0 + 64, ky, bar);
+          } else {
+            tma_load_2d_pair(st, &tm_w0, kx, w_row, bar);
+            if (GLU) tma_load_2d_pair(st + C::A_BYTES / 2, &tm_w1, kx, w_row, bar);
+          }
           tma_load_2d_pair(st + C::A_BYTES, &tm_act, kx, act_row, bar);
         }
       }
@@ -231,7 +253,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) break;
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + (uint32_t)(b * C::ACC_COLS);
-        const uint32_t idesc = idesc_bf16_f32(256, (uint32_t)N);
+        const uint32_t idesc = idesc_bf16_f32(256, (uint32_t)N) | (AMN ? (1u << 15) : 0u);
         for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -244,8 +266,10 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
-            mma_bf16_pair(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
-                          idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_pair(d0,
+                          AMN ? sdesc_mnmajor_sw128(sa + kk * 2048, C::A_BYTES / 2, 1024)
+                              : sdesc_kmajor_sw128(sa + kk * 32),
+                          sdesc_kmajor_sw128(sb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit_pair_mc(&empty[s], 0x3);  // ring slot free in both CTAs
         }
         if (!ok) break;
@@ -274,6 +298,24 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
 #pragma unroll 1
       for (int c0 = 0; c0 < N; c0 += C::CHUNK) {
+        // SwiGLU backward: this thread's saved pre-activations, loaded before
+        // anything else so the DRAM latency overlaps the accumulator read
+        uint2 zs[EPI == kEpiSwigluBwd ? 8 : 1], gs[EPI == kEpiSwigluBwd ? 8 : 1];
+        if (EPI == kEpiSwigluBwd) {
+          const int hh = args.out_ld / 2;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int item = et + 128 * i;
+            const int col = item >> 5;
+            zs[i] = gs[i] = make_uint2(0u, 0u);
+            if (c0 + col < rows) {
+              const uint16_t* sp =
+                  args.saved + (size_t)(row0 + c0 + col) * args.out_ld + col0 + (item & 31) * 4;
+              zs[i] = __ldg(reinterpret_cast<const uint2*>(sp));
+              gs[i] = __ldg(reinterpret_cast<const uint2*>(sp + hh));
+            }
+          }
+        }
         float v[32];
         tmem_ld_32(tacc + (uint32_t)c0, v);
 #pragma unroll
@@ -318,10 +360,8 @@ __global__ void __launch_bounds__(192, 1)
                 // a = dH; with the saved pre-activations z (gate) and g (up):
                 // dZ = dH * g * SiLU'(z), dG = dH * SiLU(z)
                 const int hh = args.out_ld / 2;
-                const uint2 zb = *reinterpret_cast<const uint2*>(args.saved + row * args.out_ld +
-                                                                 col0 + jq * 4);
-                const uint2 gb = *reinterpret_cast<const uint2*>(args.saved + row * args.out_ld +
-                                                                 hh + col0 + jq * 4);
+                const uint2 zb = zs[EPI == kEpiSwigluBwd ? i : 0];
+                const uint2 gb = gs[EPI == kEpiSwigluBwd ? i : 0];
                 const float dh[4] = {a.x, a.y, a.z, a.w};
                 const float z[4] = {__uint_as_float(zb.x << 16), __uint_as_float(zb.x & 0xFFFF0000u),
                                     __uint_as_float(zb.y << 16), __uint_as_float(zb.y & 0xFFFF0000u)};
@@ -394,11 +434,11 @@ static bool pair_encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uin
 }
 
 // Grid of the pair kernel: two CTAs per co-resident cluster, at most one CTA per SM.
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool AMN>
 static int pair_grid(cudaError_t* err) {
   constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
   using C = PairCfg<GLU, STAGES>;
-  auto kern = pair_gemm_kernel<EPI, STAGES>;
+  auto kern = pair_gemm_kernel<EPI, STAGES, AMN>;
   static int cached[64] = {0};
   int dev = 0;
   *err = cudaGetDevice(&dev);
@@ -431,13 +471,13 @@ static int pair_grid(cudaError_t* err) {
   return grid;
 }
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, bool AMN = false>
 static cudaError_t run_pair_gemm(const CUtensorMap& a, const CUtensorMap& w0,
                                  const CUtensorMap& w1, const PairArgs& args, cudaStream_t st) {
   constexpr bool GLU = EPI == kEpiGlu || EPI == kEpiGluSave;
   using C = PairCfg<GLU, STAGES>;
   cudaError_t e = cudaSuccess;
-  const int grid = pair_grid<EPI, STAGES>(&e);
+  const int grid = pair_grid<EPI, STAGES, AMN>(&e);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -453,7 +493,7 @@ static cudaError_t run_pair_gemm(const CUtensorMap& a, const CUtensorMap& w0,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<EPI, STAGES>, a, w0, w1, args);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<EPI, STAGES, AMN>, a, w0, w1, args);
 }
 
 bool pair_ffn_supported(const moe_shape& s) { return s.dim % 256 == 0 && s.hidden % 128 == 0; }
@@ -473,32 +513,39 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
       !pair_encode_2d(&tm_h, h, hd, R, 128) ||
       !pair_encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 128))
     return cudaErrorInvalidValue;
-  const PairArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R, save, nullptr};
+  const PairArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R, save, nullptr,
+                    0, 0};
   cudaError_t e = save != nullptr ? run_pair_gemm<kEpiGluSave, 6>(tm_x, tm_w1, tm_w3, a1, st)
                                   : run_pair_gemm<kEpiGlu, 6>(tm_x, tm_w1, tm_w3, a1, st);
   if (e != cudaSuccess) return e;
   const PairArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 256, d, d, R, nullptr,
-                    nullptr};
+                    nullptr, 0, 0};
   return run_pair_gemm<kEpiPlain, 6>(tm_h, tm_w2, tm_w2, a2, st);
 }
 
-// out[r][j] = bf16(sum_k act[r][k] W[e][j][k]) over the grouped rows r of each
-// expert e: act [R, K], W [n, M, K] (M % 256 == 0, K % 64 == 0), out rows of
-// out_ld elements (columns j < M).  With `saved` ([R, 2M] pre-activations
-// a | g) the epilogue is the SwiGLU backward: the accumulator is dH and
-// out = [dA | dG] (out_ld = 2M).
+// out[r][j] = bf16(sum_k act[r][k] B[e][k][j]) over the grouped rows r of each
+// expert e, the weights read in their stored layout: B[e] is rows [0, w_k_rows)
+// of expert block e of w0 ([n, w_k_rows, M], row-major), followed, when
+// K == 2 * w_k_rows, by the same rows of w1.  act [R, K]; M % 256 == 0,
+// w_k_rows % 64 == 0; out rows of out_ld elements (columns j < M).  With
+// `saved` ([R, 2M] pre-activations a | g) the epilogue is the SwiGLU
+// backward: the accumulator is dH and out = [dA | dG] (out_ld = 2M).
 cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int R, int n, int M,
-                                int K, const uint16_t* w, uint16_t* out, int out_ld,
-                                const uint16_t* saved, uint32_t* err, cudaStream_t st) {
+                                int K, const uint16_t* w0, const uint16_t* w1, int w_k_rows,
+                                uint16_t* out, int out_ld, const uint16_t* saved, uint32_t* err,
+                                cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  if (M % 256 != 0 || K % 64 != 0) return cudaErrorInvalidValue;
-  CUtensorMap tm_a, tm_w;
-  if (!pair_encode_2d(&tm_a, act, K, R, 128) || !pair_encode_2d(&tm_w, w, K, (uint64_t)n * M, 128))
+  if (M % 256 != 0 || w_k_rows % 64 != 0 || w_k_rows <= 0) return cudaErrorInvalidValue;
+  if (K != w_k_rows && !(K == 2 * w_k_rows && w1 != nullptr)) return cudaErrorInvalidValue;
+  CUtensorMap tm_a, tm_w0, tm_w1;
+  const uint64_t wrows = (uint64_t)n * w_k_rows;
+  if (!pair_encode_2d(&tm_a, act, K, R, 128) || !pair_encode_2d(&tm_w0, w0, M, wrows, 64) ||
+      !pair_encode_2d(&tm_w1, w1 != nullptr ? w1 : w0, M, wrows, 64))
     return cudaErrorInvalidValue;
   const PairArgs a{offsets, out, err, kWaitLimitNs, n, K / 64, M / 256, M, out_ld, R, nullptr,
-                   saved};
-  if (saved != nullptr) return run_pair_gemm<kEpiSwigluBwd, 6>(tm_a, tm_w, tm_w, a, st);
-  return run_pair_gemm<kEpiPlain, 6>(tm_a, tm_w, tm_w, a, st);
+                   saved, w_k_rows / 64, w_k_rows};
+  if (saved != nullptr) return run_pair_gemm<kEpiSwigluBwd, 6, true>(tm_a, tm_w0, tm_w1, a, st);
+  return run_pair_gemm<kEpiPlain, 6, true>(tm_a, tm_w0, tm_w1, a, st);
 }
 
 }  // namespace moe

@@ -11,7 +11,11 @@
 // in the usual K-major, 128-byte-swizzled layout.  A pair owns a 256 x 256
 // output tile (each CTA 128 rows of P and half of the 256 rows of Q, the MMA
 // M = 256 spread over both); the accumulator (2 x 256 TMEM columns, double
-// buffered) is written out by each thread as its own fp32 output row segment.
+// buffered) is drained by four epilogue warps, each owning 32 output rows:
+// 32 accumulator columns at a time go to a per-warp shared-memory tile (fp32,
+// 128-byte swizzled, double buffered) that a TMA tensor store writes to the
+// gradient, so the 4-byte-per-element output leaves as full coalesced lines
+// while the next tile's MMAs run.
 // Work units: (expert, 256-row block of M, 256-column block of N), round robin
 // over the pairs.  An expert without tokens writes zeros.
 #include <cudaTypedefs.h>
@@ -25,10 +29,10 @@ namespace moe {
 
 struct WgradArgs {
   const int32_t* poff;  // [n + 1] padded row offsets (multiples of 64)
-  float* out0;          // rows m < m_split: out0[e][m][n]
-  float* out1;          // rows m >= m_split: out1[e][m - m_split][n] (may equal out0)
-  int64_t out_estride;  // elements per expert in out0 / out1
+  // rows m < m_split go to out0[e][m][:], the rest to out1[e][m - m_split][:]
+  // (the output tensor maps view them as [n * rows, N])
   int m_split;
+  int m_rest;           // M - m_split
   int m_blocks;         // M / 256
   int n_blocks;         // N / 256
   int N;                // output row length
@@ -39,15 +43,20 @@ struct WgradArgs {
 
 constexpr int kWgStages = 6;
 constexpr int kWgStageBytes = 2 * 128 * 128;  // 128 rows of P + 128 rows of Q (64 K each)
-constexpr int kWgSmemBytes = kWgStages * kWgStageBytes + 2048 + 1024;
+constexpr int kWgStagingBytes = 4 * 2 * 32 * 128;  // per warp: 2 x [32 rows][32 fp32]
+constexpr int kWgSmemBytes = kWgStages * kWgStageBytes + kWgStagingBytes + 1024 + 1024;
+static_assert(kWgSmemBytes <= 232448, "shared memory");
 
 __global__ void __launch_bounds__(192, 1)
     wgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_p,
-                      const __grid_constant__ CUtensorMap tm_q, const WgradArgs args) {
+                      const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_o0,
+                      const __grid_constant__ CUtensorMap tm_o1, const WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* aux = tiles + kWgStages * kWgStageBytes;
+  float* staging = reinterpret_cast<float*>(tiles + kWgStages * kWgStageBytes);
+  uint8_t* aux = tiles + kWgStages * kWgStageBytes + kWgStagingBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(aux);
   uint64_t* empty = full + kWgStages;
   uint64_t* tfull = empty + kWgStages;  // [2]
@@ -82,6 +91,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_p);
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_o0);
+    tma_prefetch_desc(&tm_o1);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
 
@@ -169,8 +180,10 @@ __global__ void __launch_bounds__(192, 1)
       pair_drain_wait_shared(drain, 0, args.err, args.limit_ns);
     }
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter = this warp's 32 output rows
     const int et = threadIdx.x - 64;
+    float* stg = staging + q * (2 * 32 * 32);  // [2][32][32], 1024-byte aligned halves
+    uint32_t chunk = 0;                        // stores issued by this warp so far
     int lt = 0;
     for (int u = pair; u < total; u += npairs, ++lt) {
       const int b = lt & 1;
@@ -181,15 +194,17 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after_sync();
       int e, mb, nb, kb0, nkb;
       decode(u, e, mb, nb, kb0, nkb);
-      const int m = mb * 256 + (int)rank * 128 + q * 32 + lane;  // this thread's output row
-      float* orow = m < args.m_split
-                        ? args.out0 + (int64_t)e * args.out_estride + (int64_t)m * args.N
-                        : args.out1 + (int64_t)e * args.out_estride +
-                              (int64_t)(m - args.m_split) * args.N;
-      float4* dst = reinterpret_cast<float4*>(orow + nb * 256);
+      const int m0 = mb * 256 + (int)rank * 128 + q * 32;  // this warp's first output row
+      const bool lo = m0 < args.m_split;
+      const CUtensorMap* tmo = lo ? &tm_o0 : &tm_o1;
+      const int y = lo ? e * args.m_split + m0 : e * args.m_rest + (m0 - args.m_split);
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 32) {
+      for (int c0 = 0; c0 < 256; c0 += 32, ++chunk) {
+        float* buf = stg + (chunk & 1u) * (32 * 32);
+        // the store issued from this buffer two chunks ago has read it
+        if (chunk >= 2 && lane == 0) bulk_wait_read_le1();
+        __syncwarp();
         float v[32];
         if (nkb > 0) {
           tmem_ld_32(tacc + (uint32_t)c0, v);
@@ -197,13 +212,24 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.0f;
         }
+        // row `lane` of the tile, 16-byte pieces at the 128-byte swizzle slots
+        float* row = buf + lane * 32;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) dst[(c0 + i) / 4] = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 2)) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmo, buf, nb * 256 + c0, y);
+          bulk_commit();
+        }
       }
       tc_fence_before_sync();
       named_bar_sync(1, 128);
       if (et == 0) mbar_arrive_cluster(smem_map_rank(smem_u32(&tempty[b]), 0));
     }
+    if (lane == 0) bulk_wait_all();  // the gradient is written before the CTA exits
   }
 
   __syncthreads();
@@ -242,14 +268,34 @@ static bool wg_encode(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 gradient [rows, cols] stored by 32 x 32 tiles, 128-byte swizzle.
+static bool wg_encode_out(CUtensorMap* tm, float* base, uint64_t cols, uint64_t rows) {
+  auto enc = wg_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // C_e = P_e^T Q_e for every expert: pT [M, rpad_ld], qT [N, rpad_ld] (bf16,
-// expert e at columns [poff[e], poff[e+1])), M and N multiples of 256.
+// expert e at columns [poff[e], poff[e+1])), M and N multiples of 256.  Rows
+// m < m_split of C_e go to out0 ([n, m_split, N] fp32), the others to out1
+// ([n, M - m_split, N]); m_split is a multiple of 128.
 cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, int rpad_ld,
                          const int32_t* poff, int n, float* out0, float* out1, int m_split,
-                         int64_t out_estride, uint32_t* err, cudaStream_t st) {
+                         uint32_t* err, cudaStream_t st) {
   if (M % 256 != 0 || N % 256 != 0 || rpad_ld % 64 != 0) return cudaErrorInvalidValue;
-  CUtensorMap tm_p, tm_q;
-  if (!wg_encode(&tm_p, pT, rpad_ld, M) || !wg_encode(&tm_q, qT, rpad_ld, N))
+  if (m_split <= 0 || m_split > M || m_split % 128 != 0) return cudaErrorInvalidValue;
+  const int m_rest = M - m_split;
+  CUtensorMap tm_p, tm_q, tm_o0, tm_o1;
+  if (!wg_encode(&tm_p, pT, rpad_ld, M) || !wg_encode(&tm_q, qT, rpad_ld, N) ||
+      !wg_encode_out(&tm_o0, out0, N, (uint64_t)n * m_split) ||
+      !wg_encode_out(&tm_o1, m_rest > 0 ? out1 : out0, N,
+                     (uint64_t)n * (m_rest > 0 ? m_rest : m_split)))
     return cudaErrorInvalidValue;
   static int grids[64] = {0};
   int dev = 0;
@@ -278,8 +324,7 @@ cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, i
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     grid = 2 * clusters < (num_sms() & ~1) ? 2 * clusters : (num_sms() & ~1);
   }
-  const WgradArgs a{poff, out0, out1, out_estride, m_split, M / 256, N / 256, N, n, err,
-                    kWaitLimitNs};
+  const WgradArgs a{poff, m_split, m_rest, M / 256, N / 256, N, n, err, kWaitLimitNs};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(192);
@@ -294,7 +339,7 @@ cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, i
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, wgrad_pair_kernel, tm_p, tm_q, a);
+  return cudaLaunchKernelEx(&cfg, wgrad_pair_kernel, tm_p, tm_q, tm_o0, tm_o1, a);
 }
 
 }  // namespace moe
