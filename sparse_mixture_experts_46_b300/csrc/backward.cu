@@ -1,6 +1,6 @@
 // backward.cu -- the layer backward's CUDA-core kernels: the gradients of the
-// gated combine and of the router, the transposes that feed the weight-gradient
-// GEMMs, and the final input gradient ("Mixtral of Experts" section 2.1; the
+// gated combine and of the router, the zeroing of the padding rows between the
+// expert groups, and the final input gradient ("Mixtral of Experts" section 2.1; the
 // gradient of y = sum_k G(x)_k E_k(x) with the routing held fixed).
 //
 //   combine:  dO[row(t,k)] = g[t,k] dy[t]            (bf16, grouped rows)
@@ -8,9 +8,10 @@
 //   router:   dl[t,k] = g[t,k] (dg[t,k] - sum_j g[t,j] dg[t,j])
 //             dW_g[:, e] = sum over the rows r of expert e of x_perm[r] dl[r]
 //   input:    dx[t] = sum_k (dx_perm[row(t,k)] + dl[t,k] W_g[:, e_k])
-//   transposes with each expert's rows padded to a multiple of 64 (zeros), so
-//   that a weight gradient sum_r P[r] Q[r]^T over an expert's rows is a GEMM
-//   over whole 64-row K blocks.
+// The backward groups its rows with every expert's group starting on a
+// multiple of 64 rows; the padding rows of the grouped activations are zeroed
+// here, so that a weight gradient sum_r P[r]^T Q[r] over an expert's group is
+// a GEMM over whole 64-row K blocks.
 #include "device.cuh"
 #include "internal.h"
 
@@ -34,53 +35,40 @@ __device__ __forceinline__ uint4 pack8b(const float* f) {
 
 }  // namespace
 
-// poff[e] = sum over e' < e of round_up(count_e', 64); poff[n] = total padded rows.
-__global__ void __launch_bounds__(kMaxExperts) pad_offsets_kernel(const int32_t* __restrict__ offsets,
-                                                                  int n, int R,
-                                                                  int32_t* __restrict__ poff) {
-  __shared__ int s_scan[33];
+// Zero rows [offsets[e] + counts[e], offsets[e+1]) of each buffer (<= 63 rows
+// per expert).  Grid: (n * 64, 3): block (e, i) clears padding row i of expert
+// e (if there is one) in the buffer blockIdx.y picks.
+struct PadBufs {
+  uint16_t* p[3];
+  int cols[3];
+};
+
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int32_t* __restrict__ offsets,
+                                                            const int32_t* __restrict__ counts,
+                                                            int rows, const PadBufs bufs) {
   pdl_wait();
   pdl_launch_dependents();
-  const int e = threadIdx.x;
-  int padded = 0;
-  if (e < n) {
-    const int lo = min(max(offsets[e], 0), R);
-    const int hi = min(max(offsets[e + 1], lo), R);
-    padded = (hi - lo + 63) & ~63;
-  }
-  int total = 0;
-  const int ex = block_exclusive_scan(padded, s_scan, &total);
-  if (e < n) poff[e] = ex;
-  if (e == 0) poff[n] = total;
+  const int e = blockIdx.x >> 6;
+  uint16_t* base = bufs.p[blockIdx.y];
+  const int cols = bufs.cols[blockIdx.y];
+  if (base == nullptr) return;
+  const int lo = min(max(offsets[e] + counts[e], 0), rows);
+  const int hi = min(max(offsets[e + 1], lo), rows);
+  const int r = lo + (int)(blockIdx.x & 63);
+  if (r >= hi) return;
+  uint4* row = reinterpret_cast<uint4*>(base + (size_t)r * cols);
+  for (int i = threadIdx.x; i < (cols >> 3); i += blockDim.x) row[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Grouped activations [R, C] (expert e's rows at [offsets[e], offsets[e+1]))
-// -> dst [C, Rpad] with expert e's rows at columns [poff[e], poff[e] + count)
-// and zeros up to poff[e+1].  Grid: (C / 64, Rpad_max / 64).
-__global__ void __launch_bounds__(256) transpose_grouped_kernel(const uint16_t* __restrict__ src,
-                                                                int C, int src_ld,
-                                                                const int32_t* __restrict__ offsets,
-                                                                const int32_t* __restrict__ poff,
-                                                                int n, int R,
-                                                                uint16_t* __restrict__ dst,
-                                                                int dst_ld) {
-  __shared__ uint16_t tile[64][66];
+// wgT[e][j] = wg[j][e]: the router weight with each expert's column as a
+// contiguous row, for the input gradient's 16-byte loads.
+__global__ void __launch_bounds__(256) transpose_wg_kernel(const uint16_t* __restrict__ wg, int d,
+                                                           int n, uint16_t* __restrict__ wgT) {
   pdl_wait();
   pdl_launch_dependents();
-  const int c0 = blockIdx.x * 64, p0 = blockIdx.y * 64;
-  if (p0 >= poff[n]) return;  // beyond the padded rows of this call
-  const int e = find_expert(poff, n, p0);
-  const int lo = min(max(offsets[e], 0), R);
-  const int hi = min(max(offsets[e + 1], lo), R);
-  const int r0 = lo + (p0 - poff[e]);  // first source row of this 64-row tile
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int r = i >> 6, c = i & 63;
-    tile[r][c] = (r0 + r < hi && c0 + c < C) ? src[(int64_t)(r0 + r) * src_ld + c0 + c] : 0;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int c = i >> 6, r = i & 63;
-    if (c0 + c < C) dst[(int64_t)(c0 + c) * dst_ld + p0 + r] = tile[r][c];
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d * n; i += gridDim.x * blockDim.x) {
+    const int e = i / d, j = i - e * d;
+    wgT[i] = wg[(size_t)j * n + e];
   }
 }
 
@@ -89,7 +77,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
                                                           const uint16_t* __restrict__ y_perm,
                                                           const int32_t* __restrict__ slot_row,
                                                           const float* __restrict__ gates, int T,
-                                                          int K, int d, int R,
+                                                          int K, int d, int rows,
                                                           uint16_t* __restrict__ dO,
                                                           float* __restrict__ dg) {
   const int lane = threadIdx.x & 31;
@@ -101,7 +89,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
     const int row = slot_row[a];
     const float g = gates[a];
     float acc = 0.0f;
-    if ((unsigned)row < (unsigned)R) {
+    if ((unsigned)row < (unsigned)rows) {
       const uint4* dyr = reinterpret_cast<const uint4*>(dy + (size_t)t * d);
       const uint4* yr = reinterpret_cast<const uint4*>(y_perm + (size_t)row * d);
       uint4* outr = reinterpret_cast<uint4*>(dO + (size_t)row * d);
@@ -128,7 +116,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
 __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict__ gates,
                                                          const float* __restrict__ dg,
                                                          const int32_t* __restrict__ slot_row,
-                                                         int T, int K, int R,
+                                                         int T, int K, int rows,
                                                          float* __restrict__ dl,
                                                          float* __restrict__ dl_perm) {
   pdl_wait();
@@ -140,39 +128,64 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict
       const float v = gates[t * K + k] * (dg[t * K + k] - s);
       dl[t * K + k] = v;
       const int row = slot_row[t * K + k];
-      if ((unsigned)row < (unsigned)R) dl_perm[row] = v;
+      if ((unsigned)row < (unsigned)rows) dl_perm[row] = v;
     }
   }
 }
 
-// dW_g[j][e] = sum over the rows r of expert e, ascending, of x_perm[r][j] dl_perm[r].
-// Grid: (d / 256, n); thread j of the block owns one column.
-__global__ void __launch_bounds__(256) router_wgrad_kernel(const uint16_t* __restrict__ x_perm,
-                                                           const float* __restrict__ dl_perm,
-                                                           const int32_t* __restrict__ offsets,
-                                                           int d, int n, int R,
-                                                           float* __restrict__ dwg) {
+// dW_g[j][e] = sum over the rows r of expert e's group of x_perm[r][j] dl_perm[r].
+// Grid: (d / 256, n), 512 threads: warp w takes rows lo + w, lo + w + 16, ...
+// of the group, each lane 8 consecutive columns (one 16-byte load per row);
+// the 16 warps' partial sums are then added in warp order, so the result does
+// not depend on timing.
+constexpr int kRwgWarps = 16;
+
+__global__ void __launch_bounds__(kRwgWarps * 32) router_wgrad_kernel(
+    const uint16_t* __restrict__ x_perm, const float* __restrict__ dl_perm,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int d, int n,
+    int rows, float* __restrict__ dwg) {
+  __shared__ float part[kRwgWarps][256];
   pdl_wait();
   pdl_launch_dependents();
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
   const int e = blockIdx.y;
-  if (j >= d) return;
-  const int lo = min(max(offsets[e], 0), R);
-  const int hi = min(max(offsets[e + 1], lo), R);
-  float acc = 0.0f;
-#pragma unroll 8
-  for (int r = lo; r < hi; ++r)
-    acc = fmaf(__uint_as_float((uint32_t)x_perm[(size_t)r * d + j] << 16), dl_perm[r], acc);
-  dwg[(size_t)j * n + e] = acc;
+  const int j0 = blockIdx.x * 256 + lane * 8;  // this lane's 8 columns
+  const int lo = min(max(offsets[e], 0), rows);
+  const int hi = min(lo + max(counts[e], 0), rows);
+  float acc[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) acc[u] = 0.0f;
+  if (j0 < d) {
+#pragma unroll 4
+    for (int r = lo + w; r < hi; r += kRwgWarps) {
+      float f[8];
+      unpack8b(__ldg(reinterpret_cast<const uint4*>(x_perm + (size_t)r * d + j0)), f);
+      const float l = __ldg(dl_perm + r);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = fmaf(f[u], l, acc[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) part[w][lane * 8 + u] = acc[u];
+  __syncthreads();
+  if (threadIdx.x < 256) {
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    float sum = 0.0f;
+#pragma unroll
+    for (int v = 0; v < kRwgWarps; ++v) sum += part[v][threadIdx.x];
+    if (j < d) dwg[(size_t)j * n + e] = sum;
+  }
 }
 
-// dx[t] = bf16( sum_k (dx_perm[row(t,k)] + dl[t,k] W_g[:, e_k]) ), k ascending.
+// dx[t] = bf16( sum_k (dx_perm[row(t,k)] + dl[t,k] W_g[:, e_k]) ), k ascending
+// (wgT: W_g transposed, [n, d]).
 __global__ void __launch_bounds__(256) input_grad_kernel(const uint16_t* __restrict__ dx_perm,
                                                          const int32_t* __restrict__ slot_row,
                                                          const int32_t* __restrict__ ids,
                                                          const float* __restrict__ dl,
-                                                         const uint16_t* __restrict__ wg, int T,
-                                                         int K, int d, int n, int R,
+                                                         const uint16_t* __restrict__ wgT, int T,
+                                                         int K, int d, int n, int rows,
                                                          uint16_t* __restrict__ dx) {
   pdl_wait();
   pdl_launch_dependents();
@@ -190,16 +203,16 @@ __global__ void __launch_bounds__(256) input_grad_kernel(const uint16_t* __restr
       const int e = ids[t * K + k];
       const float l = dl[t * K + k];
       float f[8];
-      if ((unsigned)row < (unsigned)R) {
+      if ((unsigned)row < (unsigned)rows) {
         unpack8b(__ldg(reinterpret_cast<const uint4*>(dx_perm + (size_t)row * d) + v), f);
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] += f[u];
       }
       if ((unsigned)e < (unsigned)n) {
+        float w[8];
+        unpack8b(__ldg(reinterpret_cast<const uint4*>(wgT + (size_t)e * d) + v), w);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          acc[u] = fmaf(l, __uint_as_float((uint32_t)__ldg(wg + (size_t)(v * 8 + u) * n + e) << 16),
-                        acc[u]);
+        for (int u = 0; u < 8; ++u) acc[u] = fmaf(l, w[u], acc[u]);
       }
     }
     reinterpret_cast<uint4*>(dx + (size_t)t * d)[v] = pack8b(acc);
@@ -213,48 +226,50 @@ static int cap_blocks(int64_t want) {
   return (int)(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
-cudaError_t launch_pad_offsets(const int32_t* offsets, int n, int R, int32_t* poff,
-                               cudaStream_t st) {
-  return launch_pdl(pad_offsets_kernel, dim3(1), dim3(kMaxExperts), 0, st, offsets, n, R, poff);
-}
-
-cudaError_t launch_transpose_grouped(const uint16_t* src, int C, int src_ld,
-                                     const int32_t* offsets, const int32_t* poff, int n, int R,
-                                     int rpad_max, uint16_t* dst, int dst_ld, cudaStream_t st) {
-  const dim3 grid((unsigned)((C + 63) / 64), (unsigned)(rpad_max / 64));
-  return launch_pdl(transpose_grouped_kernel, grid, dim3(256), 0, st, src, C, src_ld, offsets,
-                    poff, n, R, dst, dst_ld);
+cudaError_t launch_zero_pad_rows(const int32_t* offsets, const int32_t* counts, int n, int rows,
+                                 uint16_t* b0, int c0, uint16_t* b1, int c1, uint16_t* b2, int c2,
+                                 cudaStream_t st) {
+  if (c0 % 8 != 0 || c1 % 8 != 0 || c2 % 8 != 0) return cudaErrorInvalidValue;
+  const PadBufs bufs{{b0, b1, b2}, {c0, c1, c2}};
+  return launch_pdl(zero_pad_rows_kernel, dim3((unsigned)n * 64, 3), dim3(256), 0, st, offsets,
+                    counts, rows, bufs);
 }
 
 cudaError_t launch_combine_bwd(const moe_shape& s, const uint16_t* dy, const uint16_t* y_perm,
-                               const int32_t* slot_row, const float* gates, uint16_t* dO,
-                               float* dg, cudaStream_t st) {
+                               const int32_t* slot_row, const float* gates, int rows,
+                               uint16_t* dO, float* dg, cudaStream_t st) {
   const int A = s.T * s.top_k;
   return launch_pdl(combine_bwd_kernel, dim3((unsigned)cap_blocks((A + 7) / 8)), dim3(256), 0, st,
-                    dy, y_perm, slot_row, gates, s.T, s.top_k, s.dim, A, dO, dg);
+                    dy, y_perm, slot_row, gates, s.T, s.top_k, s.dim, rows, dO, dg);
 }
 
 cudaError_t launch_router_bwd(const moe_shape& s, const float* gates, const float* dg,
-                              const int32_t* slot_row, float* dl, float* dl_perm,
+                              const int32_t* slot_row, int rows, float* dl, float* dl_perm,
                               cudaStream_t st) {
   return launch_pdl(router_bwd_kernel, dim3((unsigned)cap_blocks((s.T + 255) / 256)), dim3(256), 0,
-                    st, gates, dg, slot_row, s.T, s.top_k, s.T * s.top_k, dl, dl_perm);
+                    st, gates, dg, slot_row, s.T, s.top_k, rows, dl, dl_perm);
 }
 
 cudaError_t launch_router_wgrad(const moe_shape& s, const uint16_t* x_perm, const float* dl_perm,
-                                const int32_t* offsets, float* dwg, cudaStream_t st) {
+                                const int32_t* offsets, const int32_t* counts, int rows,
+                                float* dwg, cudaStream_t st) {
+  if (s.dim % 8 != 0) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((s.dim + 255) / 256), (unsigned)s.n_experts);
-  return launch_pdl(router_wgrad_kernel, grid, dim3(256), 0, st, x_perm, dl_perm, offsets, s.dim,
-                    s.n_experts, s.T * s.top_k, dwg);
+  return launch_pdl(router_wgrad_kernel, grid, dim3(kRwgWarps * 32), 0, st, x_perm, dl_perm,
+                    offsets, counts, s.dim, s.n_experts, rows, dwg);
 }
 
 cudaError_t launch_input_grad(const moe_shape& s, const uint16_t* dx_perm, const int32_t* slot_row,
-                              const int32_t* ids, const float* dl, const uint16_t* wg, uint16_t* dx,
-                              cudaStream_t st) {
+                              const int32_t* ids, const float* dl, const uint16_t* wg,
+                              uint16_t* wgT, int rows, uint16_t* dx, cudaStream_t st) {
+  const int dn = s.dim * s.n_experts;
+  cudaError_t e = launch_pdl(transpose_wg_kernel, dim3((unsigned)cap_blocks((dn + 255) / 256)),
+                             dim3(256), 0, st, wg, s.dim, s.n_experts, wgT);
+  if (e != cudaSuccess) return e;
   const int64_t total = (int64_t)s.T * (s.dim / 8);
   return launch_pdl(input_grad_kernel, dim3((unsigned)cap_blocks((total + 255) / 256)), dim3(256),
-                    0, st, dx_perm, slot_row, ids, dl, wg, s.T, s.top_k, s.dim, s.n_experts,
-                    s.T * s.top_k, dx);
+                    0, st, dx_perm, slot_row, ids, dl, (const uint16_t*)wgT, s.T, s.top_k, s.dim,
+                    s.n_experts, rows, dx);
 }
 
 }  // namespace moe

@@ -121,18 +121,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_scan, int* tot
 // owns rows [s_off[e], s_end[e]) (clamped into [0, rows_total]), split into
 // s_tiles[e] token tiles of `tok_tile` rows; its work units are
 // s_start[e] .. s_start[e+1] (tiles x `w_units` weight tiles, expert-major).
+// The group of expert e ends at offsets[e + 1], or, with `counts` (groups
+// padded apart), at offsets[e] + counts[e].
 // Every thread of the block calls it; s_scan is 33 ints of shared memory.
 __device__ __forceinline__ void build_tile_schedule(const int32_t* offsets, int n, int rows_total,
                                                     int tok_tile, int w_units, int* s_off,
                                                     int* s_end, int* s_tiles, int* s_start,
-                                                    int* s_scan) {
+                                                    int* s_scan, const int32_t* counts = nullptr) {
   int carry = 0;
   for (int base = 0; base < n; base += blockDim.x) {
     const int e = base + (int)threadIdx.x;
     int units = 0;
     if (e < n) {
       const int lo = min(max(offsets[e], 0), rows_total);
-      const int hi = min(max(offsets[e + 1], lo), rows_total);
+      const int end = counts != nullptr ? lo + max(counts[e], 0) : offsets[e + 1];
+      const int hi = min(max(end, lo), rows_total);
       const int tt = (hi - lo + tok_tile - 1) / tok_tile;
       s_off[e] = lo;
       s_end[e] = hi;

@@ -71,10 +71,20 @@ cudaError_t launch_rmsnorm(const moe_shape& s, const uint16_t* x, float eps, uin
                            cudaStream_t st);
 // Read (synchronously) and clear the library's router error word.
 cudaError_t router_err_read_clear(uint32_t* word);
+// Rows a grouping of R assignments over n experts can occupy when every
+// group starts on a multiple of `pad` rows.
+constexpr int permute_padded_rows(int R, int n, int pad) {
+  return (R + n * (pad - 1) + pad - 1) / pad * pad;
+}
+// Expert grouping.  pad > 1: groups start on multiples of `pad` (offsets hold
+// the padded starts, counts_out must be non-null); perm_src and x_perm then
+// hold rows_alloc >= permute_padded_rows(R, n, pad) rows, the padding rows of
+// x_perm are zeros.
 cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
                            int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
-                           uint16_t* x_perm, int nchunks, cudaStream_t st);
+                           uint16_t* x_perm, int nchunks, cudaStream_t st, int pad = 1,
+                           int rows_alloc = 0);
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* slot_row,
                            const float* gates, const uint16_t* residual, uint16_t* y,
                            cudaStream_t st);
@@ -89,38 +99,47 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
 // CTA-pair variant (weights on the MMA M side, cta_group::2); requires
 // pair_ffn_supported(s).
 bool pair_ffn_supported(const moe_shape& s);
-// save (nullable): [R, 2 * hidden] receives the gate/up pre-activations a | g.
+// save (nullable): [rows, 2 * hidden] receives the gate/up pre-activations
+// a | g.  counts (nullable): padded groups, expert e's rows are
+// [offsets[e], offsets[e] + counts[e]) of rows_alloc rows (0: R).
 cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
                                    const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
                                    const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
-                                   uint32_t* err, cudaStream_t st, uint16_t* save = nullptr);
+                                   uint32_t* err, cudaStream_t st, uint16_t* save = nullptr,
+                                   const int32_t* counts = nullptr, int rows_alloc = 0);
 // out[r][j] = bf16(sum_k act[r][k] B_e[k][j]) per expert group (CTA-pair GEMM),
 // B_e = rows of w0's expert block (then of w1's when K = 2 w_k_rows) in their
 // stored [k][j] layout; with `saved` ([R, 2M] pre-activations a | g) the SwiGLU
-// backward: out = [dA | dG].
-cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int R, int n, int M,
-                                int K, const uint16_t* w0, const uint16_t* w1, int w_k_rows,
+// backward: out = [dA | dG].  counts: as for launch_expert_ffn_pair (R rows).
+cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets,
+                                const int32_t* counts, int R, int n, int M, int K,
+                                const uint16_t* w0, const uint16_t* w1, int w_k_rows,
                                 uint16_t* out, int out_ld, const uint16_t* saved, uint32_t* err,
                                 cudaStream_t st);
-// Backward pass building blocks (backward.cu, wgrad_gemm.cu).
-cudaError_t launch_pad_offsets(const int32_t* offsets, int n, int R, int32_t* poff,
-                               cudaStream_t st);
-cudaError_t launch_transpose_grouped(const uint16_t* src, int C, int src_ld,
-                                     const int32_t* offsets, const int32_t* poff, int n, int R,
-                                     int rpad_max, uint16_t* dst, int dst_ld, cudaStream_t st);
+// Backward pass building blocks (backward.cu, wgrad_gemm.cu).  The grouped
+// buffers hold `rows` rows, expert e's group at [offsets[e], offsets[e] +
+// counts[e]) with offsets[e] a multiple of 64 (padded grouping).
+// Zero the padding rows [offsets[e] + counts[e], offsets[e+1]) of up to three
+// grouped bf16 buffers (null entries skipped).
+cudaError_t launch_zero_pad_rows(const int32_t* offsets, const int32_t* counts, int n, int rows,
+                                 uint16_t* b0, int c0, uint16_t* b1, int c1, uint16_t* b2, int c2,
+                                 cudaStream_t st);
 cudaError_t launch_combine_bwd(const moe_shape& s, const uint16_t* dy, const uint16_t* y_perm,
-                               const int32_t* slot_row, const float* gates, uint16_t* dO,
-                               float* dg, cudaStream_t st);
+                               const int32_t* slot_row, const float* gates, int rows,
+                               uint16_t* dO, float* dg, cudaStream_t st);
 cudaError_t launch_router_bwd(const moe_shape& s, const float* gates, const float* dg,
-                              const int32_t* slot_row, float* dl, float* dl_perm,
+                              const int32_t* slot_row, int rows, float* dl, float* dl_perm,
                               cudaStream_t st);
 cudaError_t launch_router_wgrad(const moe_shape& s, const uint16_t* x_perm, const float* dl_perm,
-                                const int32_t* offsets, float* dwg, cudaStream_t st);
+                                const int32_t* offsets, const int32_t* counts, int rows,
+                                float* dwg, cudaStream_t st);
+// wgT: [n, dim] scratch for the transposed router weight.
 cudaError_t launch_input_grad(const moe_shape& s, const uint16_t* dx_perm, const int32_t* slot_row,
-                              const int32_t* ids, const float* dl, const uint16_t* wg, uint16_t* dx,
-                              cudaStream_t st);
-cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, int rpad_ld,
-                         const int32_t* poff, int n, float* out0, float* out1, int m_split,
+                              const int32_t* ids, const float* dl, const uint16_t* wg,
+                              uint16_t* wgT, int rows, uint16_t* dx, cudaStream_t st);
+// C_e = P_e^T Q_e over expert e's padded group of rows: p [rows, M], q [rows, N].
+cudaError_t launch_wgrad(const uint16_t* p, const uint16_t* q, int M, int N, int rows,
+                         const int32_t* offsets, int n, float* out0, float* out1, int m_split,
                          uint32_t* err, cudaStream_t st);
 
 // Routing statistics (slot_counts [K * n], repeats [2]); zeroes both first.

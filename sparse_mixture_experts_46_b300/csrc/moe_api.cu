@@ -69,14 +69,12 @@ WsLayout ws_layout(const moe_shape* s) {
 }
 
 // Workspace of moe_layer_backward: the recomputed forward (with the gate/up
-// pre-activations), the activation gradients and the transposed operands of
-// the weight-gradient GEMMs.
+// pre-activations) and the activation gradients, all in the padded grouping.
 struct BwdLayout {
-  size_t err, ids, gates, offsets, chunk_hist, chunk_base, perm_src, slot_row, poff;
-  size_t x_perm, h, ab, y_perm, dO, dab, dx_perm, dg, dl, dl_perm;
-  size_t dOT, hT, dabT, xT;
+  size_t err, ids, gates, counts, offsets, chunk_hist, chunk_base, perm_src, slot_row;
+  size_t x_perm, h, ab, y_perm, dO, dab, dx_perm, dg, dl, dl_perm, wgT;
   size_t total;
-  int nchunks, rpad;
+  int nchunks, rows;  // rows: grouped rows, every expert's group padded to 64
 };
 
 static BwdLayout bwd_layout(const moe_shape* s) {
@@ -84,8 +82,8 @@ static BwdLayout bwd_layout(const moe_shape* s) {
   const size_t T = (size_t)s->T, R = T * (size_t)s->top_k, n = (size_t)s->n_experts;
   const size_t d = (size_t)s->dim, h = (size_t)s->hidden;
   L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
-  L.rpad = (int)((R + 63 * n + 63) / 64 * 64);  // every expert's rows padded to 64
-  const size_t rp = (size_t)L.rpad;
+  L.rows = permute_padded_rows((int)R, (int)n, 64);
+  const size_t rp = (size_t)L.rows;
   size_t off = kWsControlBytes;
   L.err = 0;
   auto take = [&](size_t bytes) {
@@ -95,33 +93,32 @@ static BwdLayout bwd_layout(const moe_shape* s) {
   };
   L.ids = take(R * 4);
   L.gates = take(R * 4);
+  L.counts = take(n * 4);
   L.offsets = take((n + 1) * 4);
   L.chunk_hist = take((size_t)L.nchunks * n * 4);
   L.chunk_base = take((size_t)L.nchunks * n * 4);
-  L.perm_src = take(R * 4);
+  L.perm_src = take(rp * 4);
   L.slot_row = take(R * 4);
-  L.poff = take((n + 1) * 4);
-  L.x_perm = take(R * d * 2);
-  L.h = take(R * h * 2);
-  L.ab = take(R * 2 * h * 2);
-  L.y_perm = take(R * d * 2);
-  L.dO = take(R * d * 2);
-  L.dab = take(R * 2 * h * 2);
-  L.dx_perm = take(R * d * 2);
+  L.x_perm = take(rp * d * 2);
+  L.h = take(rp * h * 2);
+  L.ab = take(rp * 2 * h * 2);
+  L.y_perm = take(rp * d * 2);
+  L.dO = take(rp * d * 2);
+  L.dab = take(rp * 2 * h * 2);
+  L.dx_perm = take(rp * d * 2);
   L.dg = take(R * 4);
   L.dl = take(R * 4);
-  L.dl_perm = take(R * 4);
-  L.dOT = take(d * rp * 2);
-  L.hT = take(h * rp * 2);
-  L.dabT = take(2 * h * rp * 2);
-  L.xT = take(d * rp * 2);
+  L.dl_perm = take(rp * 4);
+  L.wgT = take(n * d * 2);
   L.total = off;
   return L;
 }
 
 static bool backward_supported(const moe_shape* s) {
-  return shape_supported(s) && s->dim % 256 == 0 && s->hidden % 256 == 0 &&
-         (int64_t)s->T * s->top_k * 2 * s->hidden < (int64_t(1) << 31);
+  if (!shape_supported(s) || s->dim % 256 != 0 || s->hidden % 256 != 0) return false;
+  const int64_t R = (int64_t)s->T * s->top_k;
+  const int64_t rows = R + 64 * (int64_t)s->n_experts;  // bound of the padded grouping
+  return rows * 2 * s->hidden < (int64_t(1) << 31);
 }
 
 }  // namespace moe
@@ -310,7 +307,7 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const moe_shape& s = *shape;
-  const int T = s.T, K = s.top_k, n = s.n_experts, d = s.dim, h = s.hidden, R = T * K;
+  const int T = s.T, n = s.n_experts, d = s.dim, h = s.hidden;
   uint32_t* err = at<uint32_t>(ws, L.err);
   const int64_t nw = (int64_t)n * h * d;  // elements of one expert-weight tensor
   if (T == 0) {
@@ -323,9 +320,10 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   }
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* gates = at<float>(ws, L.gates);
+  int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* slot_row = at<int32_t>(ws, L.slot_row);
-  int32_t* poff = at<int32_t>(ws, L.poff);
+  const int rows = L.rows;
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* hb = at<uint16_t>(ws, L.h);
   uint16_t* ab = at<uint16_t>(ws, L.ab);
@@ -336,42 +334,38 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x, const m
   float* dg = at<float>(ws, L.dg);
   float* dl = at<float>(ws, L.dl);
   float* dl_perm = at<float>(ws, L.dl_perm);
-  uint16_t* dOT = at<uint16_t>(ws, L.dOT);
-  uint16_t* hT = at<uint16_t>(ws, L.hT);
-  uint16_t* dabT = at<uint16_t>(ws, L.dabT);
-  uint16_t* xT = at<uint16_t>(ws, L.xT);
 
 #define MOE_TRY(call)                           \
   do {                                          \
     const cudaError_t e_ = (call);              \
     if (e_ != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
-  // forward, recomputed: routing, grouping, expert FFN keeping the pre-activations
+  // forward, recomputed: routing, grouping (every expert's group starting on a
+  // multiple of 64 rows), expert FFN keeping the pre-activations
   MOE_TRY(launch_router(s, x, w_gate, ids, gates, nullptr, nullptr, 0.0f, err, st));
-  MOE_TRY(launch_permute(s, x, ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
+  MOE_TRY(launch_permute(s, x, ids, counts, offsets, at<int32_t>(ws, L.chunk_hist),
                          at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src), slot_row,
-                         x_perm, L.nchunks, st));
-  MOE_TRY(launch_expert_ffn_pair(s, x_perm, offsets, w1, w3, w2, hb, y_perm, err, st, ab));
+                         x_perm, L.nchunks, st, 64, rows));
+  MOE_TRY(launch_expert_ffn_pair(s, x_perm, offsets, w1, w3, w2, hb, y_perm, err, st, ab, counts,
+                                 rows));
   // gated combine and router
-  MOE_TRY(launch_combine_bwd(s, dy, y_perm, slot_row, gates, dO, dg, st));
-  MOE_TRY(launch_router_bwd(s, gates, dg, slot_row, dl, dl_perm, st));
-  MOE_TRY(launch_router_wgrad(s, x_perm, dl_perm, offsets, dw_gate, st));
+  MOE_TRY(launch_combine_bwd(s, dy, y_perm, slot_row, gates, rows, dO, dg, st));
+  MOE_TRY(launch_router_bwd(s, gates, dg, slot_row, rows, dl, dl_perm, st));
+  MOE_TRY(launch_router_wgrad(s, x_perm, dl_perm, offsets, counts, rows, dw_gate, st));
   // dH = dO W2 -> [dA | dG] (SwiGLU backward from the saved pre-activations);
   // the weights are read in their stored layout (reduction over their rows)
-  MOE_TRY(launch_pair_rowgemm(dO, offsets, R, n, h, d, w2, nullptr, d, dab, 2 * h, ab, err, st));
+  MOE_TRY(launch_pair_rowgemm(dO, offsets, counts, rows, n, h, d, w2, nullptr, d, dab, 2 * h, ab,
+                              err, st));
   // dX_perm = dA W1 + dG W3
-  MOE_TRY(launch_pair_rowgemm(dab, offsets, R, n, d, 2 * h, w1, w3, h, dx_perm, d, nullptr, err,
-                              st));
-  MOE_TRY(launch_input_grad(s, dx_perm, slot_row, ids, dl, w_gate, dx, st));
-  // weight gradients over each expert's padded rows
-  MOE_TRY(launch_pad_offsets(offsets, n, R, poff, st));
-  MOE_TRY(launch_transpose_grouped(dO, d, d, offsets, poff, n, R, L.rpad, dOT, L.rpad, st));
-  MOE_TRY(launch_transpose_grouped(hb, h, h, offsets, poff, n, R, L.rpad, hT, L.rpad, st));
-  MOE_TRY(launch_transpose_grouped(dab, 2 * h, 2 * h, offsets, poff, n, R, L.rpad, dabT, L.rpad,
-                                   st));
-  MOE_TRY(launch_transpose_grouped(x_perm, d, d, offsets, poff, n, R, L.rpad, xT, L.rpad, st));
-  MOE_TRY(launch_wgrad(dOT, hT, d, h, L.rpad, poff, n, dw2, dw2, d, err, st));
-  MOE_TRY(launch_wgrad(dabT, xT, 2 * h, d, L.rpad, poff, n, dw1, dw3, h, err, st));
+  MOE_TRY(launch_pair_rowgemm(dab, offsets, counts, rows, n, d, 2 * h, w1, w3, h, dx_perm, d,
+                              nullptr, err, st));
+  MOE_TRY(launch_input_grad(s, dx_perm, slot_row, ids, dl, w_gate, at<uint16_t>(ws, L.wgT), rows,
+                            dx, st));
+  // weight gradients over each expert's padded group (x_perm's padding rows
+  // are zero from the grouping; dO's, H's and [dA | dG]'s are zeroed here)
+  MOE_TRY(launch_zero_pad_rows(offsets, counts, n, rows, dO, d, hb, h, dab, 2 * h, st));
+  MOE_TRY(launch_wgrad(dO, hb, d, h, rows, offsets, n, dw2, dw2, d, err, st));
+  MOE_TRY(launch_wgrad(dab, x_perm, 2 * h, d, rows, offsets, n, dw1, dw3, h, err, st));
 #undef MOE_TRY
   return MOE_OK;
 }

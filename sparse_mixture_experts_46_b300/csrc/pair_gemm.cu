@@ -79,6 +79,7 @@ struct PairArgs {
   // K blocks [0, k_split), then the same rows of tm_w1's for the rest
   int k_split;
   int w_k_rows;
+  const int32_t* counts;   // nullable: padded groups end at offsets[e] + counts[e]
 };
 
 template <bool GLU, int STAGES>
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(192, 1)
   pdl_wait();
   pdl_launch_dependents();
   build_tile_schedule(args.offsets, n, args.rows_total, C::TOK_TILE, args.w_tiles, s_off, s_end,
-                      s_tok_tiles, s_tile_start, s_scan);
+                      s_tok_tiles, s_tile_start, s_scan, args.counts);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
@@ -296,25 +297,36 @@ __global__ void __launch_bounds__(192, 1)
       decode_tile(t, e, wt, row0, rows, N);
       const int col0 = wt * 2 * C::OUT_COLS + (int)rank * C::OUT_COLS;  // output column base
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      // SwiGLU backward: this thread's saved pre-activations of chunk c0 (8
+      // items of 4 columns), fetched one chunk ahead so their DRAM latency
+      // hides behind the previous chunk's work
+      constexpr int NS = EPI == kEpiSwigluBwd ? 8 : 1;
+      uint2 zs[NS], gs[NS], zn[NS], gn[NS];
+      auto fetch_saved = [&](int c, uint2* z, uint2* g) {
+        const int hh = args.out_ld / 2;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+          const int item = et + 128 * i;
+          const int col = item >> 5;
+          z[i] = g[i] = make_uint2(0u, 0u);
+          if (c + col < rows) {
+            const uint16_t* sp =
+                args.saved + (size_t)(row0 + c + col) * args.out_ld + col0 + (item & 31) * 4;
+            z[i] = __ldg(reinterpret_cast<const uint2*>(sp));
+            g[i] = __ldg(reinterpret_cast<const uint2*>(sp + hh));
+          }
+        }
+      };
+      if (EPI == kEpiSwigluBwd) fetch_saved(0, zn, gn);
 #pragma unroll 1
       for (int c0 = 0; c0 < N; c0 += C::CHUNK) {
-        // SwiGLU backward: this thread's saved pre-activations, loaded before
-        // anything else so the DRAM latency overlaps the accumulator read
-        uint2 zs[EPI == kEpiSwigluBwd ? 8 : 1], gs[EPI == kEpiSwigluBwd ? 8 : 1];
         if (EPI == kEpiSwigluBwd) {
-          const int hh = args.out_ld / 2;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int item = et + 128 * i;
-            const int col = item >> 5;
-            zs[i] = gs[i] = make_uint2(0u, 0u);
-            if (c0 + col < rows) {
-              const uint16_t* sp =
-                  args.saved + (size_t)(row0 + c0 + col) * args.out_ld + col0 + (item & 31) * 4;
-              zs[i] = __ldg(reinterpret_cast<const uint2*>(sp));
-              gs[i] = __ldg(reinterpret_cast<const uint2*>(sp + hh));
-            }
+          for (int i = 0; i < NS; ++i) {
+            zs[i] = zn[i];
+            gs[i] = gn[i];
           }
+          if (c0 + C::CHUNK < N) fetch_saved(c0 + C::CHUNK, zn, gn);
         }
         float v[32];
         tmem_ld_32(tacc + (uint32_t)c0, v);
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(192, 1)
                 float dz[4], dg[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                  const float sg = 1.0f / (1.0f + __expf(-z[u]));
+                  const float sg = __fdividef(1.0f, 1.0f + __expf(-z[u]));
                   dz[u] = dh[u] * g[u] * sg * (1.0f + z[u] * (1.0f - sg));
                   dg[u] = dh[u] * z[u] * sg;
                 }
@@ -501,9 +513,10 @@ bool pair_ffn_supported(const moe_shape& s) { return s.dim % 256 == 0 && s.hidde
 cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
                                    const int32_t* offsets, const uint16_t* w1, const uint16_t* w3,
                                    const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
-                                   uint32_t* err, cudaStream_t st, uint16_t* save) {
-  const int R = s.T * s.top_k;
-  if (R == 0) return cudaSuccess;
+                                   uint32_t* err, cudaStream_t st, uint16_t* save,
+                                   const int32_t* counts, int rows_alloc) {
+  if (s.T * s.top_k == 0) return cudaSuccess;
+  const int R = rows_alloc > 0 ? rows_alloc : s.T * s.top_k;
   if (!pair_ffn_supported(s)) return cudaErrorInvalidValue;
   const int d = s.dim, hd = s.hidden, n = s.n_experts;
   CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
@@ -514,12 +527,12 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
       !pair_encode_2d(&tm_w2, w2, hd, (uint64_t)n * d, 128))
     return cudaErrorInvalidValue;
   const PairArgs a1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R, save, nullptr,
-                    0, 0};
+                    0, 0, counts};
   cudaError_t e = save != nullptr ? run_pair_gemm<kEpiGluSave, 6>(tm_x, tm_w1, tm_w3, a1, st)
                                   : run_pair_gemm<kEpiGlu, 6>(tm_x, tm_w1, tm_w3, a1, st);
   if (e != cudaSuccess) return e;
   const PairArgs a2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 256, d, d, R, nullptr,
-                    nullptr, 0, 0};
+                    nullptr, 0, 0, counts};
   return run_pair_gemm<kEpiPlain, 6>(tm_h, tm_w2, tm_w2, a2, st);
 }
 
@@ -529,9 +542,12 @@ cudaError_t launch_expert_ffn_pair(const moe_shape& s, const uint16_t* x_perm,
 // K == 2 * w_k_rows, by the same rows of w1.  act [R, K]; M % 256 == 0,
 // w_k_rows % 64 == 0; out rows of out_ld elements (columns j < M).  With
 // `saved` ([R, 2M] pre-activations a | g) the epilogue is the SwiGLU
-// backward: the accumulator is dH and out = [dA | dG] (out_ld = 2M).
-cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int R, int n, int M,
-                                int K, const uint16_t* w0, const uint16_t* w1, int w_k_rows,
+// backward: the accumulator is dH and out = [dA | dG] (out_ld = 2M).  With
+// `counts` the groups are padded apart: expert e's rows are [offsets[e],
+// offsets[e] + counts[e]) of the R rows of act / out.
+cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets,
+                                const int32_t* counts, int R, int n, int M, int K,
+                                const uint16_t* w0, const uint16_t* w1, int w_k_rows,
                                 uint16_t* out, int out_ld, const uint16_t* saved, uint32_t* err,
                                 cudaStream_t st) {
   if (R == 0) return cudaSuccess;
@@ -543,7 +559,7 @@ cudaError_t launch_pair_rowgemm(const uint16_t* act, const int32_t* offsets, int
       !pair_encode_2d(&tm_w1, w1 != nullptr ? w1 : w0, M, wrows, 64))
     return cudaErrorInvalidValue;
   const PairArgs a{offsets, out, err, kWaitLimitNs, n, K / 64, M / 256, M, out_ld, R, nullptr,
-                   saved, w_k_rows / 64, w_k_rows};
+                   saved, w_k_rows / 64, w_k_rows, counts};
   if (saved != nullptr) return run_pair_gemm<kEpiSwigluBwd, 6, true>(tm_a, tm_w0, tm_w1, a, st);
   return run_pair_gemm<kEpiPlain, 6, true>(tm_a, tm_w0, tm_w1, a, st);
 }

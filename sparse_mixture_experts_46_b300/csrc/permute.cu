@@ -15,6 +15,10 @@
 //   4. gather:  x_perm[row] = x[perm_src[row]], 16-byte vector moves, one
 //               thread per slice.
 // For small T*K (decode batches) steps 1-3 run as one single-block kernel.
+// With pad > 1 every expert's group starts on a multiple of `pad` rows
+// (offsets are then the padded starts and the group of e ends at
+// offsets[e] + counts[e]); the padding rows get perm_src = -1 and are written
+// as zeros by the gather.
 #include "device.cuh"
 #include "internal.h"
 
@@ -39,10 +43,11 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_hist_kernel(const int32
 
 // One block of kMaxExperts threads: thread e owns expert e.
 __global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(const int32_t* __restrict__ hist,
-                                                                   int nchunks, int n,
+                                                                   int nchunks, int n, int pad,
                                                                    int32_t* __restrict__ counts,
                                                                    int32_t* __restrict__ offsets,
-                                                                   int32_t* __restrict__ chunk_base) {
+                                                                   int32_t* __restrict__ chunk_base,
+                                                                   int32_t* __restrict__ perm_src) {
   __shared__ int s_scan[33];
   const int e = threadIdx.x;
   int total = 0;
@@ -56,12 +61,14 @@ __global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(const int32_t
     }
   }
   // exclusive prefix over experts (threads >= n contribute 0)
+  const int seg = (total + pad - 1) / pad * pad;
   int all = 0;
-  const int excl = block_exclusive_scan(total, s_scan, &all);
+  const int excl = block_exclusive_scan(seg, s_scan, &all);
   if (e < n) {
     if (counts) counts[e] = total;
     offsets[e] = excl;
     for (int c = 0; c < nchunks; ++c) chunk_base[(size_t)c * n + e] += excl;
+    for (int r = excl + total; r < excl + seg; ++r) perm_src[r] = -1;  // padding rows
   }
   if (e == 0) offsets[n] = all;
 }
@@ -96,23 +103,27 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
 }
 
 // x_perm[r, :] = x[perm_src[r], :]; one thread per 16-byte slice of a row
-// (flat grid), so every row move is in flight at once.
+// (flat grid), so every row move is in flight at once.  Rows whose perm_src
+// is not a token (padding; or ids outside [0, n)) are written as zeros.  With
+// `rows_used` (device, padded groups) rows at or past *rows_used are skipped.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm_src,
                                                           int R, int d, int T,
+                                                          const int32_t* __restrict__ rows_used,
                                                           uint16_t* __restrict__ x_perm) {
   const int vec = d >> 3;
-  const int64_t total = (int64_t)R * vec;
   pdl_wait();
   pdl_launch_dependents();
+  const int rows = rows_used != nullptr ? min(max(*rows_used, 0), R) : R;
+  const int64_t total = (int64_t)rows * vec;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(i / vec);
     const int v = (int)(i - (int64_t)r * vec);
     const int t = __ldg(perm_src + r);
-    if ((unsigned)t >= (unsigned)T) continue;  // only reachable with ids outside [0, n)
     reinterpret_cast<uint4*>(x_perm + (size_t)r * d)[v] =
-        __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v);
+        (unsigned)t < (unsigned)T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v)
+                                  : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -123,7 +134,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 constexpr int kSmallPermute = 2048;
 
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids,
-                                                            int R, int K, int n,
+                                                            int R, int K, int n, int pad,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ perm_src,
@@ -147,12 +158,14 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   __syncthreads();
   {
     const int total = tid < n ? s_cnt[tid] : 0;
+    const int seg = (total + pad - 1) / pad * pad;
     int all = 0;
-    const int excl = block_exclusive_scan(total, s_scan, &all);
+    const int excl = block_exclusive_scan(seg, s_scan, &all);
     if (tid < n) {
       s_base[tid] = excl;
       offsets[tid] = excl;
       if (counts) counts[tid] = total;
+      for (int r = excl + total; r < excl + seg; ++r) perm_src[r] = -1;  // padding rows
     }
     if (tid == 0) offsets[n] = all;
   }
@@ -188,19 +201,23 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
 cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
                            int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
-                           uint16_t* x_perm, int nchunks, cudaStream_t st) {
+                           uint16_t* x_perm, int nchunks, cudaStream_t st, int pad,
+                           int rows_alloc) {
   const int R = s.T * s.top_k;
+  if (pad < 1) return cudaErrorInvalidValue;
+  if (pad > 1 && rows_alloc < permute_padded_rows(R, s.n_experts, pad))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   if (R <= kSmallPermute) {
     e = launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, st, ids, R, s.top_k, s.n_experts,
-                   counts_out, offsets, perm_src, slot_row);
+                   pad, counts_out, offsets, perm_src, slot_row);
     if (e != cudaSuccess) return e;
   } else {
     e = launch_pdl(permute_hist_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,
                    s.n_experts, chunk_hist);
     if (e != cudaSuccess) return e;
     e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, (const int32_t*)chunk_hist,
-                   nchunks, s.n_experts, counts_out, offsets, chunk_base);
+                   nchunks, s.n_experts, pad, counts_out, offsets, chunk_base, perm_src);
     if (e != cudaSuccess) return e;
     e = launch_pdl(permute_scatter_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,
                    s.top_k, s.n_experts, (const int32_t*)chunk_base, perm_src, slot_row);
@@ -208,12 +225,15 @@ cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t*
   }
   if (R == 0) return cudaSuccess;
   if (x_perm != nullptr) {
-    const int64_t total = (int64_t)R * (s.dim / 8);
+    const int rows = pad > 1 ? rows_alloc : R;
+    const int64_t total = (int64_t)rows * (s.dim / 8);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
     e = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, x,
-                   (const int32_t*)perm_src, R, s.dim, s.T, x_perm);
+                   (const int32_t*)perm_src, rows, s.dim, s.T,
+                   pad > 1 ? (const int32_t*)(offsets + s.n_experts) : (const int32_t*)nullptr,
+                   x_perm);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

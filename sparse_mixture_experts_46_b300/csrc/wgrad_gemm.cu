@@ -5,10 +5,13 @@
 // dW3_e = dG_e^T X_e, the expert weights' gradients summed over the tokens
 // routed to the expert).
 //
-// Both operands arrive transposed, [M, Rpad] and [N, Rpad], with each expert's
-// rows padded with zeros to a multiple of 64 (columns [poff[e], poff[e+1])),
-// so the reduction over an expert's tokens is a run of whole 64-wide K blocks
-// in the usual K-major, 128-byte-swizzled layout.  A pair owns a 256 x 256
+// Both operands are read as the grouped activations themselves, P [rows, M]
+// and Q [rows, N], in which every expert's group starts on a multiple of 64
+// rows and is followed by zero rows up to the next group ([offsets[e],
+// offsets[e+1])): the reduction over an expert's tokens is a run of whole
+// 64-row K blocks, each landing by TMA as 64 rows of 128 bytes (64 columns),
+// 128-byte swizzled -- the MN-major operand layout for both A and B, so no
+// transposed copy is made.  A pair owns a 256 x 256
 // output tile (each CTA 128 rows of P and half of the 256 rows of Q, the MMA
 // M = 256 spread over both); the accumulator (2 x 256 TMEM columns, double
 // buffered) is drained by four epilogue warps, each owning 32 output rows:
@@ -28,7 +31,7 @@
 namespace moe {
 
 struct WgradArgs {
-  const int32_t* poff;  // [n + 1] padded row offsets (multiples of 64)
+  const int32_t* offsets;  // [n + 1] group starts (multiples of 64); padding rows are zero
   // rows m < m_split go to out0[e][m][:], the rest to out1[e][m - m_split][:]
   // (the output tensor maps view them as [n * rows, N])
   int m_split;
@@ -42,7 +45,7 @@ struct WgradArgs {
 };
 
 constexpr int kWgStages = 6;
-constexpr int kWgStageBytes = 2 * 128 * 128;  // 128 rows of P + 128 rows of Q (64 K each)
+constexpr int kWgStageBytes = 2 * 128 * 128;  // 128 columns of P + 128 of Q (64 K rows each)
 constexpr int kWgStagingBytes = 4 * 2 * 32 * 128;  // per warp: 2 x [32 rows][32 fp32]
 constexpr int kWgSmemBytes = kWgStages * kWgStageBytes + kWgStagingBytes + 1024 + 1024;
 static_assert(kWgSmemBytes <= 232448, "shared memory");
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
 
-  pdl_wait();  // the transposed operands and poff are written by earlier kernels
+  pdl_wait();  // the operands and the offsets are written by earlier kernels
   pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
@@ -111,8 +114,8 @@ __global__ void __launch_bounds__(192, 1)
     const int local = u - e * per_expert;
     mb = local / args.n_blocks;
     nb = local - mb * args.n_blocks;
-    kb0 = args.poff[e] >> 6;
-    nkb = (args.poff[e + 1] - args.poff[e]) >> 6;
+    kb0 = args.offsets[e] >> 6;
+    nkb = max(args.offsets[e + 1] - args.offsets[e], 0) >> 6;
   };
 
   if (warp == 0) {
@@ -134,9 +137,11 @@ __global__ void __launch_bounds__(192, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kWgStageBytes);
           const uint32_t bar = smem_map_rank(smem_u32(&full[s]), 0);
           uint8_t* st = tiles + s * kWgStageBytes;
-          const int kx = (kb0 + kb) * 64;
-          tma_load_2d_pair(st, &tm_p, kx, prow, bar);
-          tma_load_2d_pair(st + 128 * 128, &tm_q, kx, qrow, bar);
+          const int ky = (kb0 + kb) * 64;  // 64 grouped rows = one K block
+          tma_load_2d_pair(st, &tm_p, prow, ky, bar);
+          tma_load_2d_pair(st + 64 * 128, &tm_p, prow + 64, ky, bar);
+          tma_load_2d_pair(st + 128 * 128, &tm_q, qrow, ky, bar);
+          tma_load_2d_pair(st + 192 * 128, &tm_q, qrow + 64, ky, bar);
         }
       }
       if (rank == 0)
@@ -148,7 +153,8 @@ __global__ void __launch_bounds__(192, 1)
     if (rank == 0 && lane == 0) {
       int it = 0, lt = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_bf16_f32(256, 256);
+      // A and B both MN-major
+      const uint32_t idesc = idesc_bf16_f32(256, 256) | (1u << 15) | (1u << 16);
       for (int u = pair; ok && u < total; u += npairs, ++lt) {
         int e, mb, nb, kb0, nkb;
         decode(u, e, mb, nb, kb0, nkb);
@@ -169,8 +175,9 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sb = sa + 128 * 128;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_pair(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
-                          idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_pair(d0, sdesc_mnmajor_sw128(sa + kk * 2048, 64 * 128, 1024),
+                          sdesc_mnmajor_sw128(sb + kk * 2048, 64 * 128, 1024), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
           mma_commit_pair_mc(&empty[s], 0x3);
         }
         if (!ok) break;
@@ -256,12 +263,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 wg_encoder() {
   return fn;
 }
 
+// Grouped bf16 activations [rows, cols], boxes of 64 columns x 64 rows.
 static bool wg_encode(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows) {
   auto enc = wg_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, 64};
   const cuuint32_t estr[2] = {1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -281,18 +289,19 @@ static bool wg_encode_out(CUtensorMap* tm, float* base, uint64_t cols, uint64_t 
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// C_e = P_e^T Q_e for every expert: pT [M, rpad_ld], qT [N, rpad_ld] (bf16,
-// expert e at columns [poff[e], poff[e+1])), M and N multiples of 256.  Rows
+// C_e = P_e^T Q_e for every expert: p [rows, M], q [rows, N] (bf16, expert
+// e's group at rows [offsets[e], offsets[e+1]), offsets multiples of 64, the
+// rows past the group's tokens zero), M and N multiples of 256.  Rows
 // m < m_split of C_e go to out0 ([n, m_split, N] fp32), the others to out1
 // ([n, M - m_split, N]); m_split is a multiple of 128.
-cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, int rpad_ld,
-                         const int32_t* poff, int n, float* out0, float* out1, int m_split,
+cudaError_t launch_wgrad(const uint16_t* p, const uint16_t* q, int M, int N, int rows,
+                         const int32_t* offsets, int n, float* out0, float* out1, int m_split,
                          uint32_t* err, cudaStream_t st) {
-  if (M % 256 != 0 || N % 256 != 0 || rpad_ld % 64 != 0) return cudaErrorInvalidValue;
+  if (M % 256 != 0 || N % 256 != 0 || rows % 64 != 0 || rows <= 0) return cudaErrorInvalidValue;
   if (m_split <= 0 || m_split > M || m_split % 128 != 0) return cudaErrorInvalidValue;
   const int m_rest = M - m_split;
   CUtensorMap tm_p, tm_q, tm_o0, tm_o1;
-  if (!wg_encode(&tm_p, pT, rpad_ld, M) || !wg_encode(&tm_q, qT, rpad_ld, N) ||
+  if (!wg_encode(&tm_p, p, M, rows) || !wg_encode(&tm_q, q, N, rows) ||
       !wg_encode_out(&tm_o0, out0, N, (uint64_t)n * m_split) ||
       !wg_encode_out(&tm_o1, m_rest > 0 ? out1 : out0, N,
                      (uint64_t)n * (m_rest > 0 ? m_rest : m_split)))
@@ -324,7 +333,7 @@ cudaError_t launch_wgrad(const uint16_t* pT, const uint16_t* qT, int M, int N, i
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     grid = 2 * clusters < (num_sms() & ~1) ? 2 * clusters : (num_sms() & ~1);
   }
-  const WgradArgs a{poff, m_split, m_rest, M / 256, N / 256, N, n, err, kWaitLimitNs};
+  const WgradArgs a{offsets, m_split, m_rest, M / 256, N / 256, N, n, err, kWaitLimitNs};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(192);

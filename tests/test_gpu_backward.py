@@ -48,7 +48,7 @@ def close(name, got, ref, tol):
                                 [float(ref[tuple(i)]) for i in idx]))
 
 
-def run_backward(cfg, L, dy):
+def run_backward(cfg, L, dy, poison_ws=False):
     moe = lib()
     n, d, h = cfg.n_experts, cfg.dim, cfg.hidden
     f32 = dict(dtype=torch.float32, device="cuda")
@@ -58,6 +58,11 @@ def run_backward(cfg, L, dy):
     dw3 = torch.full((n, h, d), float("nan"), **f32)
     dw2 = torch.full((n, d, h), float("nan"), **f32)
     ws = moe.new_backward_workspace(cfg)
+    if poison_ws:
+        # every byte past the control region 0xFF: bf16 NaN in every grouped
+        # buffer, so a padding row that is read without being zeroed poisons
+        # the weight gradients
+        ws[65536:].fill_(0xFF)
     if cfg.T > 0:
         x, dyd = dev_bf16(L.x), dev_bf16(dy)
     else:
@@ -69,11 +74,11 @@ def run_backward(cfg, L, dy):
                 dw1=dw1.cpu().numpy(), dw3=dw3.cpu().numpy(), dw2=dw2.cpu().numpy())
 
 
-def check_backward(cfg):
+def check_backward(cfg, poison_ws=False):
     L = mi.make_layer(cfg)
     filter_x(cfg, L.x, L.wg, L.shift)
     dy = mi.gen_x(cfg.replace(seed=cfg.seed + 1))
-    got = run_backward(cfg, L, dy)
+    got = run_backward(cfg, L, dy, poison_ws)
     ref = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy)
     matched = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy, bf16_points=True)
     for name in ("dx", "dwg", "dw1", "dw3", "dw2"):
@@ -91,6 +96,19 @@ def test_backward_wider_dims_and_ragged_groups():
     # dim 512, hidden 768: several 256-wide tiles per expert in every GEMM
     cfg = mi.Config("bwd", T=333, dim=512, hidden=768, seed=46300)
     check_backward(cfg)
+
+
+def test_backward_groups_without_padding():
+    # top 2 of 2 experts: both groups hold exactly T = 128 rows (two whole
+    # 64-row blocks), so no padding row lies between them
+    cfg = mi.Config("bwd", T=128, dim=256, hidden=256, n_experts=2, top_k=2, seed=46304)
+    check_backward(cfg)
+
+
+def test_backward_ignores_stale_workspace():
+    # ragged groups (96 tokens, top 2 of 8) in a workspace full of NaN bytes
+    cfg = mi.Config("bwd", T=96, dim=256, hidden=256, seed=46305)
+    check_backward(cfg, poison_ws=True)
 
 
 def test_backward_zero_tokens_gives_zero_weight_gradients():
