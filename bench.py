@@ -55,7 +55,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", choices=sorted(WORKLOADS) + ["backward"], default="mixtral")
-    p.add_argument("--profile", choices=[DECODE, PREFILL, "fine_decode", "fine"], default=None,
+    p.add_argument("--profile", choices=[DECODE, PREFILL, "skew", "fine_decode", "fine",
+                                         "backward"],
+                   default=None,
                    help="no timing: run W warm-up + K layer calls of one workload (for ncu)")
     return p.parse_args()
 
@@ -387,11 +389,41 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def run_profile_backward(args):
+    """W + K moe_layer_backward calls on a reduced case for section captures:
+    Mixtral dims with 2 experts, top 1, T=2048 (about 1024 rows per expert, as in
+    the T=4096 top-2-of-8 batch; 2.4 GB on the device)."""
+    import torch
+    import sparse_mixture_experts_46_b300 as moe
+    import moe_inputs as mi
+    cfg = mi.Config("bwd_profile", T=2048, dim=4096, hidden=14336, n_experts=2, top_k=1,
+                    seed=46400)
+    L = mi.make_layer(cfg)
+    x, wg, w1, w3, w2 = (to_dev(a) for a in (L.x, L.wg, L.w1, L.w3, L.w2))
+    dy = to_dev(mi.gen_x(cfg.replace(seed=cfg.seed + 1)))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    n, d, h = cfg.n_experts, cfg.dim, cfg.hidden
+    dx = torch.empty((cfg.T, d), dtype=torch.bfloat16, device="cuda")
+    grads = [torch.empty((d, n), **f32), torch.empty((n, h, d), **f32),
+             torch.empty((n, h, d), **f32), torch.empty((n, d, h), **f32)]
+    ws = moe.new_backward_workspace(cfg)
+    for _ in range(args.warmup + args.steps):
+        moe.moe_layer_backward(cfg, x, wg, w1, w3, w2, dy, dx, *grads, ws)
+    torch.cuda.synchronize()
+    st = moe.moe_check_error(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: %d" % st)
+    print("profile case backward: %d calls ok" % (args.warmup + args.steps))
+
+
 def run_profile_case(args):
     """One workload only, W + K layer calls through moe_layer_forward, no timing:
     the small, single-layer case that ncu captures use."""
     import torch
     import sparse_mixture_experts_46_b300 as moe
+    if args.profile == "backward":
+        run_profile_backward(args)
+        return
     cfg, L = load_layer(args.profile)
     b = Buffers(cfg, L)
     for _ in range(args.warmup + args.steps):

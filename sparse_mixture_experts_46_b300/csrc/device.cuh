@@ -123,11 +123,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_scan, int* tot
 // s_start[e] .. s_start[e+1] (tiles x `w_units` weight tiles, expert-major).
 // The group of expert e ends at offsets[e + 1], or, with `counts` (groups
 // padded apart), at offsets[e] + counts[e].
+// With s_span (nullable): s_span[e] = token tiles per L2 block of expert e --
+// all of its tiles when its activation rows (row_bytes each) fit in
+// `l2_budget` bytes, else the fewest equal blocks that do (see pair_gemm.cu).
 // Every thread of the block calls it; s_scan is 33 ints of shared memory.
 __device__ __forceinline__ void build_tile_schedule(const int32_t* offsets, int n, int rows_total,
                                                     int tok_tile, int w_units, int* s_off,
                                                     int* s_end, int* s_tiles, int* s_start,
-                                                    int* s_scan, const int32_t* counts = nullptr) {
+                                                    int* s_scan, const int32_t* counts = nullptr,
+                                                    int* s_span = nullptr, int64_t row_bytes = 0,
+                                                    int64_t l2_budget = 0) {
   int carry = 0;
   for (int base = 0; base < n; base += blockDim.x) {
     const int e = base + (int)threadIdx.x;
@@ -141,6 +146,14 @@ __device__ __forceinline__ void build_tile_schedule(const int32_t* offsets, int 
       s_end[e] = hi;
       s_tiles[e] = tt;
       units = tt * w_units;
+      if (s_span != nullptr) {
+        const int64_t bytes = (int64_t)(hi - lo) * row_bytes;
+        int64_t blocks = l2_budget > 0 ? (bytes + l2_budget - 1) / l2_budget : 1;
+        if (blocks > tt) blocks = tt;
+        if (blocks < 1) blocks = 1;
+        const int nb = (int)blocks;
+        s_span[e] = tt > 0 ? (tt + nb - 1) / nb : 1;
+      }
     }
     int total = 0;
     const int ex = block_exclusive_scan(units, s_scan, &total);

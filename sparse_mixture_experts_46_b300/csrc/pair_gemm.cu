@@ -33,7 +33,13 @@
 // The accumulator is double-buffered (2 x 256 TMEM columns), so the epilogue
 // of tile i overlaps the main loop of tile i+1.  Tiles (expert, weight tile,
 // token tile) are scheduled from the device-resident offsets, expert-major,
-// then weight tile, then token tile, round-robin over the pairs.
+// then weight tile, then token tile, round-robin over the pairs.  An expert
+// whose activation rows exceed an L2 budget (kL2Budget: a skewed routing can
+// send tens of thousands of rows to one expert) has its token tiles split into
+// equal blocks that fit, walked block by block (block, weight tile, token
+// tile): each block's rows stay in L2 while every weight tile passes over
+// them, instead of all the expert's rows being re-read from HBM once per
+// weight tile.
 //
 // The same kernel serves the activation-gradient GEMMs of the backward pass
 // with the weights read in their stored layout (AMN): there the reduction
@@ -82,6 +88,10 @@ struct PairArgs {
   const int32_t* counts;   // nullable: padded groups end at offsets[e] + counts[e]
 };
 
+// Activation bytes of one expert that the tile order keeps resident in L2
+// (about a third of the 126 MB L2; weights in flight and outputs share it).
+constexpr int64_t kL2Budget = 40ll << 20;
+
 template <bool GLU, int STAGES>
 struct PairCfg {
   static constexpr int BK = 64;                  // bf16 per 128-byte row
@@ -94,8 +104,8 @@ struct PairCfg {
   static constexpr int ACC_COLS = 256;           // TMEM columns per accumulator buffer
   static constexpr int CHUNK = 32;               // accumulator columns per epilogue step
   static constexpr int STAGING_BYTES = CHUNK * 128 * 4;
-  // barriers and flags (1 KB), then the tile schedule: 4 tables of kMaxExperts + 1
-  static constexpr int AUX_BYTES = 1024 + 4 * (kMaxExperts + 1) * 4 + 33 * 4;
+  // barriers and flags (1 KB), then the tile schedule: 5 tables of kMaxExperts + 1
+  static constexpr int AUX_BYTES = 1024 + 5 * (kMaxExperts + 1) * 4 + 33 * 4;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + AUX_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -141,7 +151,8 @@ __global__ void __launch_bounds__(192, 1)
   int* s_tok_tiles = s_tile_start + kMaxExperts + 1;         // [kMaxExperts + 1]
   int* s_off = s_tok_tiles + kMaxExperts + 1;                // [kMaxExperts + 1]
   int* s_end = s_off + kMaxExperts + 1;                      // [kMaxExperts + 1]
-  int* s_scan = s_end + kMaxExperts + 1;                     // [33]
+  int* s_span = s_end + kMaxExperts + 1;                     // [kMaxExperts + 1]
+  int* s_scan = s_span + kMaxExperts + 1;                    // [33]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -176,7 +187,8 @@ __global__ void __launch_bounds__(192, 1)
   pdl_wait();
   pdl_launch_dependents();
   build_tile_schedule(args.offsets, n, args.rows_total, C::TOK_TILE, args.w_tiles, s_off, s_end,
-                      s_tok_tiles, s_tile_start, s_scan, args.counts);
+                      s_tok_tiles, s_tile_start, s_scan, args.counts, s_span,
+                      (int64_t)args.k_blocks * C::BK * 2, kL2Budget);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
@@ -186,13 +198,20 @@ __global__ void __launch_bounds__(192, 1)
   const int total_tiles = s_tile_start[n];
   const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
 
-  // tile -> expert e, weight tile wt, first token row, valid rows, MMA N
+  // tile -> expert e, weight tile wt, first token row, valid rows, MMA N;
+  // the expert's tiles are blocks of s_span[e] token tiles (the last block may
+  // be shorter), each walked weight tile by weight tile
   auto decode_tile = [&](int t, int& e, int& wt, int& row0, int& rows, int& N) {
     e = find_expert(s_tile_start, n, t);
     const int local = t - s_tile_start[e];
     const int ntt = s_tok_tiles[e];
-    wt = local / ntt;
-    const int tt = local - wt * ntt;
+    const int span = s_span[e];
+    const int per_block = args.w_tiles * span;
+    const int blk = local / per_block;
+    const int rem = local - blk * per_block;
+    const int bs = min(span, ntt - blk * span);  // token tiles in this block
+    wt = rem / bs;
+    const int tt = blk * span + (rem - wt * bs);
     row0 = s_off[e] + tt * C::TOK_TILE;
     rows = min(C::TOK_TILE, s_end[e] - row0);
     N = (rows + 15) & ~15;
