@@ -67,6 +67,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+// 16-byte load from a cluster peer's shared memory (addr 16-byte aligned).
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 
 // Top-K of one token's logits l[0..16) (entries >= n are ignored) and the
 // softmax of the selected ones; writes ids / gates of token t.
@@ -301,19 +310,59 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 // 128-byte swizzled, i.e. the MN-major operand layout; the MMA is M=128 tokens
 // x N=round_up(n, 16) x K=16, B marked MN-major in the instruction descriptor
 // (matrix descriptor: 1024 bytes between 8-row feature groups, 8 KB between
-// 64-expert blocks).  One CTA per 128 tokens streams the whole model
-// dimension.  The epilogue thread of each token walks its n logits in
-// ascending expert order and keeps a sorted top-K list (strictly greater
-// displaces, so ties keep the lower index).
+// 64-expert blocks).  One CTA per 128 tokens, or, when there are too few
+// token tiles to cover the SMs (decode batches), a cluster of `split` CTAs
+// per tile, each reducing 1/split of the model dimension: every CTA writes
+// its 128 x n fp32 partial logits over its (by then idle) operand ring, and
+// CTA r adds rows [r*128/split, (r+1)*128/split) of all the cluster's partials
+// in rank order (a fixed order) through distributed shared memory.  The thread
+// of each token then walks its n logits in ascending expert order and keeps a
+// sorted top-K list (strictly greater displaces, so ties keep the lower index).
 constexpr int kRwThreads = 128;
 constexpr int kRwStages = 4;
 constexpr int kRwMaxK = 8;
 
+// Order of the top-K lists: larger logit first, equal logits by lower index.
+__device__ __forceinline__ bool rw_before(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+// A top-K list is kRwMaxK sorted slots whose first kRwMaxK - K hold (+inf, -1),
+// which nothing displaces: the K kept entries are the last slots, so the
+// current K-th best is always the last slot and most candidates are turned
+// away by one comparison (an insertion is a chain through every slot).
+__device__ __forceinline__ void rw_init(float* tv, int* ti, int K) {
+#pragma unroll
+  for (int j = 0; j < kRwMaxK; ++j) {
+    const bool pinned = j < kRwMaxK - K;
+    tv[j] = pinned ? INFINITY : -INFINITY;
+    ti[j] = pinned ? -1 : 0x7fffffff;
+  }
+}
+// Insertion without a chain through the slots: "slot j keeps its entry"
+// (the entry is before the candidate) holds for a prefix of the sorted list,
+// so every slot's new entry follows from the old list alone -- its own entry,
+// the candidate, or the entry one slot up.
+__device__ __forceinline__ void rw_insert(float* tv, int* ti, float val, int e) {
+  if (!rw_before(val, e, tv[kRwMaxK - 1], ti[kRwMaxK - 1])) return;
+  bool keep[kRwMaxK];
+#pragma unroll
+  for (int j = 0; j < kRwMaxK; ++j) keep[j] = !rw_before(val, e, tv[j], ti[j]);
+#pragma unroll
+  for (int j = kRwMaxK - 1; j >= 0; --j) {
+    if (!keep[j]) {
+      const bool here = j == 0 || keep[j - 1];
+      tv[j] = here ? val : tv[j > 0 ? j - 1 : 0];
+      ti[j] = here ? e : ti[j > 0 ? j - 1 : 0];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRwThreads, 1)
     router_tc_wide_kernel(const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_w, int T, int d, int n, int K,
-                          int nblk, int32_t* __restrict__ ids, float* __restrict__ gates,
-                          int32_t* __restrict__ counts, uint32_t* err, uint64_t limit_ns) {
+                          int nblk, int split, int kb_per_cta, int32_t* __restrict__ ids,
+                          float* __restrict__ gates, int32_t* __restrict__ counts, uint32_t* err,
+                          uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -328,9 +377,12 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int tile = blockIdx.x;
-  const int kb_total = d / 64;
+  const uint32_t rank = split > 1 ? cluster_ctarank() : 0u;
+  const int tile = blockIdx.x / split;
+  const int kb0 = (int)rank * kb_per_cta;
   const int npad = (n + 15) & ~15;
+  const int pstride = npad + 4;  // floats per token row of the partials (16-byte rows)
+  float* part = reinterpret_cast<float*>(ring);  // [128][pstride], over the ring once it is idle
 
   if (tid == 0) {
     for (int s = 0; s < kRwStages; ++s) {
@@ -353,24 +405,25 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
+  if (split > 1) cluster_sync_all();  // every peer is running before any DSMEM access
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wctl{abort_flag, err, limit_ns};
 
   if (warp == 0 && lane == 0) {
-    for (int kb = 0; kb < kb_total; ++kb) {
+    for (int kb = 0; kb < kb_per_cta; ++kb) {
       const int s = kb % kRwStages;
       const uint32_t ph = (uint32_t)(kb / kRwStages) & 1u;
       if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) break;
       uint8_t* st = ring + s * stage_bytes;
       mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-      tma_load_2d(st, &tm_x, kb * 64, tile * 128, &full[s]);
+      tma_load_2d(st, &tm_x, (kb0 + kb) * 64, tile * 128, &full[s]);
       for (int b = 0; b < nblk; ++b)
-        tma_load_2d(st + kRtTileBytes + b * 8192, &tm_w, b * 64, kb * 64, &full[s]);
+        tma_load_2d(st + kRtTileBytes + b * 8192, &tm_w, b * 64, (kb0 + kb) * 64, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)npad) | (1u << 16);  // B MN-major
-    for (int kb = 0; kb < kb_total; ++kb) {
+    for (int kb = 0; kb < kb_per_cta; ++kb) {
       const int s = kb % kRwStages;
       const uint32_t ph = (uint32_t)(kb / kRwStages) & 1u;
       if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) break;
@@ -391,54 +444,103 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   int ok = 0;
   if (lane == 0) ok = mbar_wait(tfull, 0, wctl, kErrTimeoutEpilogue) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  const int t = tile * 128 + warp * 32 + lane;
-  if (ok) {
-    tc_fence_after_sync();
-    float tv[kRwMaxK];
-    int ti[kRwMaxK];
-#pragma unroll
-    for (int j = 0; j < kRwMaxK; ++j) {
-      tv[j] = -INFINITY;
-      ti[j] = j;
-    }
-    for (int c0 = 0; c0 < npad; c0 += 16) {
-      float v[16];
+  const int r = warp * 32 + lane;  // token row inside the tile = TMEM lane
+  // every token row's logits into the partial buffer over the (idle) ring:
+  // every MMA, hence every operand read, has completed
+  if (ok) tc_fence_after_sync();
+  for (int c0 = 0; c0 < npad; c0 += 16) {
+    float v[16];
+    if (ok) {
       tmem_ld_16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);  // warp-collective
+    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float val = v[i];
-        int e = c0 + i;
-        if (e >= n || !(val == val)) continue;  // padding and NaN never enter
-        // insertion into the sorted list: a strictly greater value moves ahead
+      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    }
 #pragma unroll
-        for (int j = 0; j < kRwMaxK; ++j) {
-          if (j < K && val > tv[j]) {
-            const float fv = tv[j];
-            const int fi = ti[j];
-            tv[j] = val;
-            ti[j] = e;
-            val = fv;
-            e = fi;
-          }
+    for (int i = 0; i < 16; i += 4)
+      *reinterpret_cast<float4*>(part + r * pstride + c0 + i) =
+          make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  }
+  const int per = 128 / split;  // token rows this CTA selects for
+  const int row0 = (int)rank * per;
+  if (split > 1) {
+    cluster_sync_all();  // every CTA's partials are visible cluster-wide
+    // this CTA's token rows: the sum over the cluster in rank order, written
+    // back over its own rows (no peer reads them); one item = 4 experts of a
+    // row, every peer's 16 bytes requested before the sum
+    const int n4 = npad >> 2;
+    for (int i = tid; i < per * n4; i += kRwThreads) {
+      const int rr = row0 + i / n4;
+      const int e = (i - (i / n4) * n4) * 4;
+      const uint32_t local = smem_u32(part + rr * pstride + e);
+      float4 pv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c < split) pv[c] = ld_cluster_f32x4(smem_map_rank(local, (uint32_t)c));
+      float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (c < split) {  // rank order: a fixed summation order
+          sum.x += pv[c].x;
+          sum.y += pv[c].y;
+          sum.z += pv[c].z;
+          sum.w += pv[c].w;
         }
       }
+      *reinterpret_cast<float4*>(part + rr * pstride + e) = sum;
     }
-    if (t < T) {
-      const float v0 = tv[0];
+  }
+  __syncthreads();
+  // selection: `split` threads per token row (G = 128 / per); thread g keeps
+  // the top K of experts g, g + G, ... (NaN counts as -inf), then the G lists
+  // are merged into thread 0's; the list order is total, so the result does
+  // not depend on the order of the merge
+  {
+    const int G = split;
+    const int rl = tid / G, g = tid - (tid / G) * G;
+    const float* row = part + (row0 + rl) * pstride;
+    float tv[kRwMaxK];
+    int ti[kRwMaxK];
+    rw_init(tv, ti, K);
+    for (int e = g; e < n; e += G) {
+      const float x = row[e];
+      rw_insert(tv, ti, x == x ? x : -INFINITY, e);
+    }
+    // merge the row's G lists (consecutive lanes of one warp) as a tree of
+    // shuffles: at distance d, lane g (g % 2d == 0) takes the kept entries of
+    // lane g + d
+    for (int d = 1; d < G; d <<= 1) {
+#pragma unroll
+      for (int j = 0; j < kRwMaxK; ++j) {
+        const float pv = __shfl_down_sync(0xffffffffu, tv[j], d);
+        const int pi = __shfl_down_sync(0xffffffffu, ti[j], d);
+        if ((g & (2 * d - 1)) == 0 && j >= kRwMaxK - K) rw_insert(tv, ti, pv, pi);
+      }
+    }
+    const int t = tile * 128 + row0 + rl;
+    if (g == 0 && ok && t < T && !*abort_flag) {
+      // slot k of the output is list slot kRwMaxK - K + k
+      // the largest kept logit (the list is sorted and holds no NaN)
+      float v0 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kRwMaxK; ++j)
+        if (j >= kRwMaxK - K) v0 = fmaxf(v0, tv[j]);
       float denom = 0.0f;
 #pragma unroll
       for (int j = 0; j < kRwMaxK; ++j)
-        if (j < K) denom += expf(tv[j] - v0);
+        if (j >= kRwMaxK - K) denom += expf(tv[j] - v0);
 #pragma unroll
       for (int j = 0; j < kRwMaxK; ++j) {
-        if (j < K) {
-          ids[(size_t)t * K + j] = ti[j];
-          gates[(size_t)t * K + j] = expf(tv[j] - v0) / denom;
+        if (j >= kRwMaxK - K) {
+          const int k = j - (kRwMaxK - K);
+          ids[(size_t)t * K + k] = ti[j];
+          gates[(size_t)t * K + k] = expf(tv[j] - v0) / denom;
           if (counts != nullptr) atomicAdd(&hist[ti[j]], 1);
         }
       }
     }
   }
+  if (split > 1) cluster_sync_all();  // no CTA leaves while a peer may still read its partials
   __syncthreads();
   if (counts != nullptr)
     for (int e = tid; e < n; e += kRwThreads)
@@ -621,14 +723,36 @@ cudaError_t launch_router_wide(const moe_shape& s, const uint16_t* x, const uint
       return cudaErrorInvalidValue;
   }
   const int nblk = (s.n_experts + 63) / 64;
-  const size_t smem = 1024 + (size_t)kRwStages * (kRtTileBytes + nblk * 8192) + 2048;
+  const size_t ring = (size_t)kRwStages * (kRtTileBytes + nblk * 8192);
+  // the partial logits [128][npad + 4] fp32 reuse the ring
+  static_assert((size_t)kRwStages * (kRtTileBytes + 8192) >= 128 * (64 + 4) * 4, "partials");
+  // + barriers, flags and the count histogram
+  const size_t smem = 1024 + ring + 2048;
   cudaError_t e = cudaFuncSetAttribute(router_tc_wide_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // split the model dimension over a cluster until the grid covers the SMs
   const int tiles = (s.T + 127) / 128;
-  return launch_pdl(router_tc_wide_kernel, dim3((unsigned)tiles), dim3(kRwThreads), smem, st, tm_x,
-                    tm_w, s.T, s.dim, s.n_experts, s.top_k, nblk, ids, gates, counts, err,
-                    kWaitLimitNs);
+  const int kb = s.dim / 64;
+  int split = 1;
+  while (split < 8 && kb % (split * 2) == 0 && tiles * split * 2 <= num_sms()) split *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * split));
+  cfg.blockDim = dim3(kRwThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, router_tc_wide_kernel, tm_x, tm_w, s.T, s.dim, s.n_experts,
+                            s.top_k, nblk, split, kb / split, ids, gates, counts, err,
+                            kWaitLimitNs);
 }
 
 cudaError_t launch_rmsnorm(const moe_shape& s, const uint16_t* x, float eps, uint16_t* u,

@@ -98,6 +98,13 @@ def test_backward_wider_dims_and_ragged_groups():
     check_backward(cfg)
 
 
+def test_backward_top8_of_40_odd_tile_count():
+    # fine-grained shape: top 8 of 40 experts (wide router), hidden 1792 = 7
+    # tiles of 256, so every weight-side loop ends on an odd tile
+    cfg = mi.Config("bwd", T=48, dim=512, hidden=1792, n_experts=40, top_k=8, seed=46306)
+    check_backward(cfg)
+
+
 def test_backward_groups_without_padding():
     # top 2 of 2 experts: both groups hold exactly T = 128 rows (two whole
     # 64-row blocks), so no padding row lies between them

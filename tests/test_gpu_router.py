@@ -48,7 +48,10 @@ def layer_inputs(cfg):
     (512, 128, 8, 8), (1030, 512, 16, 16), (2049, 4096, 8, 2),
     # more than 32 experts (fine-grained MoE): the wide tensor-core router
     (200, 256, 40, 2), (1000, 512, 64, 6), (700, 256, 160, 8), (129, 128, 256, 8),
-    (1, 256, 160, 8), (64, 128, 48, 1), (600, 4096, 160, 8)])
+    (1, 256, 160, 8), (64, 128, 48, 1), (600, 4096, 160, 8),
+    # the wide router splits the model dimension over a cluster of up to 8 CTAs
+    # while the token tiles leave SMs idle; 75 tiles (9600 tokens) run unsplit
+    (16, 4096, 160, 8), (9600, 128, 40, 2)])
 def test_router_matches_oracle(T, dim, n, K):
     cfg = mi.Config("r", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=700 + T + n)
     x, wg = layer_inputs(cfg)
