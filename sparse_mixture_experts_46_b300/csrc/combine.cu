@@ -20,8 +20,10 @@ __device__ __forceinline__ void unpack8c(const uint4& v, float* f) {
 }
 
 // One thread per 16-byte slice of an output row: thread i of the flat grid
-// writes slice i % (dim/8) of token i / (dim/8); every load it issues is
-// independent, so the whole output is in flight at once.
+// writes slice i % (dim/8) of token i / (dim/8), with the loads of KC slots
+// at a time in flight together (KC: the smallest of 2, 4, 8 that covers K, so
+// top-2 keeps the registers, hence the occupancy, of a two-slot loop).
+template <int KC>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_row,
                                                       const float* __restrict__ gates,
@@ -39,14 +41,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const int row = __ldg(slot_row + (size_t)t * K + k);
-      if ((unsigned)row >= (unsigned)R) continue;
-      const float g = __ldg(gates + (size_t)t * K + k);
-      float f[8];
-      unpack8c(__ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row * d) + v), f);
+    // KC slots at a time: their row indices and gates, then their row
+    // slices, are all requested before the first is used; the sum still runs
+    // k = 0, 1, ... in order
+    for (int k0 = 0; k0 < K; k0 += KC) {
+      int row[KC];
+      float g[KC];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(g, f[j], acc[j]);
+      for (int j = 0; j < KC; ++j) {
+        const int k = k0 + j;
+        row[j] = k < K ? __ldg(slot_row + (size_t)t * K + k) : -1;
+        g[j] = k < K ? __ldg(gates + (size_t)t * K + k) : 0.0f;
+      }
+      uint4 val[KC];
+#pragma unroll
+      for (int j = 0; j < KC; ++j)
+        val[j] = (unsigned)row[j] < (unsigned)R
+                     ? __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)row[j] * d) + v)
+                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        if ((unsigned)row[j] < (unsigned)R) {
+          float f[8];
+          unpack8c(val[j], f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] = fmaf(g[j], f[u], acc[u]);
+        }
+      }
     }
     if (residual != nullptr) {
       float r[8];
@@ -71,8 +92,9 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, y_perm, slot_row,
-                    gates, residual, s.T, s.top_k, s.dim, s.T * s.top_k, y);
+  auto kern = s.top_k <= 2 ? combine_kernel<2> : (s.top_k <= 4 ? combine_kernel<4> : combine_kernel<8>);
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(256), 0, st, y_perm, slot_row, gates,
+                    residual, s.T, s.top_k, s.dim, s.T * s.top_k, y);
 }
 
 }  // namespace moe

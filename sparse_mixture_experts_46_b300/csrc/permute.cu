@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kPermuteChunk) permute_scatter_kernel(
 }
 
 // x_perm[r, :] = x[perm_src[r], :]; one thread per 16-byte slice of a row
-// (flat grid), so every row move is in flight at once.  Rows whose perm_src
+// (flat grid), four slices in flight per thread.  Rows whose perm_src
 // is not a token (padding; or ids outside [0, n)) are written as zeros.  With
 // `rows_used` (device, padded groups) rows at or past *rows_used are skipped.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
@@ -116,14 +116,27 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   pdl_launch_dependents();
   const int rows = rows_used != nullptr ? min(max(*rows_used, 0), R) : R;
   const int64_t total = (int64_t)rows * vec;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / vec);
-    const int v = (int)(i - (int64_t)r * vec);
-    const int t = __ldg(perm_src + r);
-    reinterpret_cast<uint4*>(x_perm + (size_t)r * d)[v] =
-        (unsigned)t < (unsigned)T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v)
-                                  : make_uint4(0u, 0u, 0u, 0u);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // 4 slices per round (i, i + stride, ...): their source rows, then their
+  // 16 bytes, are all requested before the first store
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    int r[4], v[4], t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      r[u] = i < total ? (int)(i / vec) : -1;
+      v[u] = i < total ? (int)(i - (int64_t)r[u] * vec) : 0;
+      t[u] = r[u] >= 0 ? __ldg(perm_src + r[u]) : -1;
+    }
+    uint4 val[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      val[u] = (unsigned)t[u] < (unsigned)T
+                   ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t[u] * d) + v[u])
+                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (r[u] >= 0) reinterpret_cast<uint4*>(x_perm + (size_t)r[u] * d)[v[u]] = val[u];
   }
 }
 

@@ -228,8 +228,9 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(
       float best = 0.0f;
       int bi = -1;
       for (int e = 0; e < n; ++e) {
-        if (!((taken >> e) & 1u) && (bi < 0 || l[e] > best)) {
-          best = l[e];
+        const float le = l[e] == l[e] ? l[e] : -INFINITY;  // NaN counts as -inf
+        if (!((taken >> e) & 1u) && (bi < 0 || le > best)) {
+          best = le;
           bi = e;
         }
       }
@@ -246,8 +247,9 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(
       float best = 0.0f;
       int bi = -1;
       for (int e = 0; e < n; ++e) {
-        if (!((taken >> e) & 1u) && (bi < 0 || l[e] > best)) {
-          best = l[e];
+        const float le = l[e] == l[e] ? l[e] : -INFINITY;  // NaN counts as -inf
+        if (!((taken >> e) & 1u) && (bi < 0 || le > best)) {
+          best = le;
           bi = e;
         }
       }

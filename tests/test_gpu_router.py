@@ -86,6 +86,26 @@ def test_wide_router_exact_ties_go_to_lower_index():
     assert counts.tolist() == [cfg.T] * 8 + [0] * 152
 
 
+@pytest.mark.parametrize("n,K", [(8, 2), (24, 2), (40, 4)])
+def test_router_nan_logit_counts_as_minus_infinity(n, K):
+    # every token's logit for expert 3 is NaN (a NaN column of W_g): all three
+    # routers (tensor-core n <= 16, CUDA-core n <= 32, wide) must route as if
+    # expert 3 did not exist
+    cfg = mi.Config("nan", T=200, dim=128, hidden=128, n_experts=n, top_k=K, seed=900 + n)
+    wg = mi.gen_router_weight(cfg)
+    keep = [e for e in range(n) if e != 3]
+    wg_rest = np.ascontiguousarray(wg[:, keep])
+    x = mi.gen_x(cfg)
+    filter_x(cfg.replace(n_experts=n - 1), x, wg_rest)
+    wg_nan = wg.copy()
+    wg_nan[:, 3] = 0x7FC0                   # bf16 quiet NaN
+    ids, gates, counts = run_router(cfg, x, wg_nan)
+    r_ids, r_gates, _ = orc.router(x, wg_rest, K)
+    assert np.array_equal(ids, np.where(r_ids >= 3, r_ids + 1, r_ids))
+    assert np.max(np.abs(gates - r_gates), initial=0.0) < 1e-5
+    assert counts[3] == 0
+
+
 def test_router_zero_tokens_clears_counts():
     cfg = mi.Config("empty", T=0, dim=128, hidden=128)
     _, _, counts = run_router(cfg, np.zeros((0, 128), np.uint16), mi.gen_router_weight(cfg))
