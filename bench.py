@@ -343,16 +343,20 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(layers, prefill_tokens):
-    """The oracle on the decode batch and a seeded sample of the prefill batch."""
+def oracle_sample(layers, prefill_tokens, decode_tokens=None, step=0):
+    """The oracle on a sample of the step's tokens: `decode_tokens` of the decode
+    batch (all of it when None) and `prefill_tokens` of the prefill batch, taken
+    from fixed seeded permutations of each batch, the window moving with `step`."""
     from oracle import moe_oracle as orc
     tokens = 0
     t0 = time.perf_counter()
     for name, (cfg, L) in layers.items():
-        if name == DECODE:
-            rows = np.arange(cfg.T)
-        else:
-            rows = np.sort(np.random.default_rng(1).choice(cfg.T, prefill_tokens, replace=False))
+        k = (cfg.T if decode_tokens is None else decode_tokens) if name == DECODE else prefill_tokens
+        k = min(k, cfg.T)
+        if k <= 0:
+            continue
+        perm = np.random.default_rng(1 if name != DECODE else 2).permutation(cfg.T)
+        rows = np.sort(perm[(step * k + np.arange(k)) % cfg.T])
         orc.moe_layer(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k)
         tokens += len(rows)
     return tokens, time.perf_counter() - t0
@@ -365,17 +369,22 @@ def run_reference(args, rank, world):
         return
     metric, dec_name, pre_name = WORKLOADS[args.workload]
     layers = {DECODE: load_layer(dec_name), PREFILL: load_layer(pre_name)}
-    prefill_tokens = 32
-    for _ in range(args.warmup):
-        oracle_sample(layers, prefill_tokens)
+    # the oracle takes ~0.15 s per token on 16 host threads: about 720 tokens
+    # over all K + W steps keeps the run near two minutes at any K
+    per_step = max(2, min(48, 720 // max(1, args.steps + args.warmup)))
+    decode_tokens = max(1, per_step // 3)
+    prefill_tokens = per_step - decode_tokens
+    for i in range(args.warmup):
+        oracle_sample(layers, prefill_tokens, decode_tokens, step=i)
     total_tok, total_s = 0, 0.0
-    for _ in range(args.steps):
-        tok, s = oracle_sample(layers, prefill_tokens)
+    for i in range(args.steps):
+        tok, s = oracle_sample(layers, prefill_tokens, decode_tokens, step=args.warmup + i)
         total_tok += tok
         total_s += s
     value = total_tok / total_s
-    sample = ("fp64 oracle per step: decode batch (16 tokens) + %d seeded prefill tokens"
-              % prefill_tokens)
+    sample = ("fp64 oracle per step: %d decode + %d prefill tokens of the step's batches "
+              "(seeded windows moving each step; %d tokens over the %d steps)"
+              % (decode_tokens, prefill_tokens, total_tok, args.steps))
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,

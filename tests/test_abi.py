@@ -92,3 +92,31 @@ def test_host_validation_returns_before_any_launch(lib):
     assert lib.moe_permute(ctypes.byref(s), *args, ctypes.c_size_t(4096), None) == 3
     assert lib.moe_status_string(3) == b"MOE_ERR_WORKSPACE_TOO_SMALL"
     assert lib.moe_status_string(5) == b"MOE_ERR_TIMEOUT"
+
+
+def test_backward_and_stats_shape_rules_and_validation(lib):
+    lib.moe_backward_workspace_bytes.restype = ctypes.c_size_t
+    vp = ctypes.c_void_p
+    # the backward needs dim and hidden multiples of 256
+    for bad in (Shape(16, 128, 256, 8, 2), Shape(16, 256, 384, 8, 2), Shape(16, 256, 256, 8, 9)):
+        assert lib.moe_backward_workspace_bytes(ctypes.byref(bad)) == 0
+    small = lib.moe_backward_workspace_bytes(ctypes.byref(Shape(16, 256, 256, 8, 2)))
+    large = lib.moe_backward_workspace_bytes(ctypes.byref(Shape(4096, 256, 256, 8, 2)))
+    # the grouped buffers hold at least T*K rows of x_perm, h, [a|g], y_perm, dO, [dA|dG], dx_perm
+    assert large > small > 0
+    assert large >= 4096 * 2 * (4 * 256 + 5 * 256) * 2
+    s = Shape(16, 256, 256, 8, 2)
+    p = [vp(0x10000 * (i + 1)) for i in range(11)]
+    # null shape / unsupported shape / null pointer / workspace too small: no launch
+    assert lib.moe_layer_backward(None, *p, vp(0x200000), ctypes.c_size_t(small), None) == 1
+    bad = Shape(16, 128, 256, 8, 2)
+    assert lib.moe_layer_backward(ctypes.byref(bad), *p, vp(0x200000), ctypes.c_size_t(small),
+                                  None) == 2
+    assert lib.moe_layer_backward(ctypes.byref(s), None, *p[1:], vp(0x200000),
+                                  ctypes.c_size_t(small), None) == 1
+    assert lib.moe_layer_backward(ctypes.byref(s), *p, vp(0x200000), ctypes.c_size_t(small - 1),
+                                  None) == 3
+    # routing statistics: null outputs and unsupported shapes return before any launch
+    assert lib.moe_routing_stats(ctypes.byref(s), vp(0x1000), None, vp(0x2000), None) == 1
+    assert lib.moe_routing_stats(ctypes.byref(Shape(16, 256, 256, 8, 9)), vp(0x1000),
+                                 vp(0x2000), vp(0x3000), None) == 2
