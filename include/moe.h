@@ -1,6 +1,7 @@
 /*
  * moe.h -- C ABI of the B300 (sm_103a) Mixtral sparse mixture-of-experts
- * layer forward.
+ * layer: the forward and its steps, the backward (routing held fixed) and the
+ * routing statistics.
  *
  * The layer ("Mixtral of Experts", section 2.1):
  *     y = sum_i G(x)_i * E_i(x),         G(x) = Softmax(TopK(x . W_g)),
@@ -22,8 +23,8 @@
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *   enqueued asynchronously on it, in order.
  * - Routing conventions: slot k of a token holds its k-th largest logit, ties
- *   broken towards the lower expert index; gates are the softmax of the K
- *   selected logits (float32).  The grouped ("permuted") row order is the
+ *   broken towards the lower expert index, a NaN logit counting as -infinity;
+ *   gates are the softmax of the K selected logits (float32).  The grouped ("permuted") row order is the
  *   stable sort of the flat assignments a = t*K + k by expert id: rows
  *   [offsets[e], offsets[e+1]) belong to expert e, tokens ascending.
  * - Supported shapes: T >= 0 (T = 0 is a no-op), 1 <= top_k <= n_experts <= 256,
