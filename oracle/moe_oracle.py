@@ -170,7 +170,8 @@ def silu_grad(a: np.ndarray) -> np.ndarray:
     return sg * (1.0 + a * (1.0 - sg))
 
 
-def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool = False):
+def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool = False,
+                       weight_grads: bool = True):
     """Gradients of the sparse MoE layer (§2.1) for an upstream gradient dy.
 
     The routing (which K experts each token uses) is held fixed: TopK is
@@ -191,44 +192,81 @@ def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool 
     kept for the backward; the expert outputs o, g_k dy, da and db, and each
     expert's input-gradient rows), everything else in fp64; the exact mode
     (default) rounds nothing.
+    weight_grads=False skips dw1 / dw3 / dw2 (returned as None), for callers
+    that only need dx and dwg of a few tokens at full model size.
     """
     rnd = (lambda v: widen_bf16(round_bf16(v))) if bf16_points else (lambda v: v)
     xf, wg = _f64(x), _f64(w_gate)
-    W1, W3, W2 = _f64(w1), _f64(w3), _f64(w2)
     g_up = _f64(dy)
     ids, gates, _ = router(xf, wg, top_k)
     T, dim = xf.shape
-    n = W1.shape[0]
+    n = np.asarray(w1).shape[0]
     dx = np.zeros_like(xf)
     dwg = np.zeros_like(wg)
-    dw1, dw3, dw2 = np.zeros_like(W1), np.zeros_like(W3), np.zeros_like(W2)
+    dw1 = dw3 = dw2 = None
+    if weight_grads:
+        dw1 = np.zeros(np.asarray(w1).shape)
+        dw3 = np.zeros(np.asarray(w3).shape)
+        dw2 = np.zeros(np.asarray(w2).shape)
     dgate = np.zeros((T, top_k))
     for e in range(n):
         tok, slot = np.nonzero(ids == e)
         if len(tok) == 0:
             continue
+        W1e, W3e, W2e = _f64(w1[e]), _f64(w3[e]), _f64(w2[e])   # one expert at a time
         xe = xf[tok]
-        a_x = xe @ W1[e].T
-        b_x = xe @ W3[e].T
+        a_x = xe @ W1e.T
+        b_x = xe @ W3e.T
         h = rnd(silu(a_x) * b_x)          # h from the unrounded pre-activations
         a, b = rnd(a_x), rnd(b_x)         # the stored pre-activations feed the backward
         s = silu(a)
-        o = rnd(h @ W2[e].T)
+        o = rnd(h @ W2e.T)
         do = rnd(gates[tok, slot][:, None] * g_up[tok])
         dgate[tok, slot] = np.sum(g_up[tok] * o, axis=1)
-        dh = do @ W2[e]
-        dw2[e] += do.T @ h
+        dh = do @ W2e
         da = rnd(dh * b * silu_grad(a))
         db = rnd(dh * s)
-        dw1[e] += da.T @ xe
-        dw3[e] += db.T @ xe
-        np.add.at(dx, tok, rnd(da @ W1[e] + db @ W3[e]))
+        if weight_grads:
+            dw2[e] += do.T @ h
+            dw1[e] += da.T @ xe
+            dw3[e] += db.T @ xe
+        np.add.at(dx, tok, rnd(da @ W1e + db @ W3e))
     dl_sel = gates * (dgate - np.sum(gates * dgate, axis=1, keepdims=True))
     dl = np.zeros((T, n))
     np.put_along_axis(dl, ids, dl_sel, axis=1)
     dwg += xf.T @ dl
     dx += dl @ wg.T
     return dict(dx=dx, dwg=dwg, dw1=dw1, dw3=dw3, dw2=dw2)
+
+
+def expert_weight_grad_units(x, w_gate, w1, w3, w2, top_k: int, dy, e: int, units):
+    """Expert e's weight gradients for a few hidden units j in ``units``, from the
+    same chain rule as ``moe_layer_backward`` (routing fixed, exact mode) but
+    evaluated on hidden units j only: dW1_e[j, :] and dW3_e[j, :] (rows of the
+    [hidden, dim] gradients) and dW2_e[:, j] (columns of the [dim, hidden]
+    gradient).  Hidden unit j of the expert needs only a_j = W1_e[j] x,
+    b_j = W3_e[j] x and dh_j = W2_e[:, j] . d o for the tokens routed to e,
+    so the cost is a few dot products per token and unit, at any model size.
+    Returns dict(dw1 [len(units), dim], dw3 [len(units), dim],
+    dw2 [dim, len(units)]), float64.
+    """
+    units = np.asarray(units)
+    xf, wg = _f64(x), _f64(w_gate)
+    g_up = _f64(dy)
+    ids, gates, _ = router(xf, wg, top_k)
+    tok, slot = np.nonzero(ids == e)
+    W1j = _f64(np.asarray(w1)[e][units])            # [u, dim]
+    W3j = _f64(np.asarray(w3)[e][units])            # [u, dim]
+    W2j = _f64(np.asarray(w2)[e][:, units])         # [dim, u]
+    xe = xf[tok]
+    a = xe @ W1j.T
+    b = xe @ W3j.T
+    h = silu(a) * b
+    do = gates[tok, slot][:, None] * g_up[tok]
+    dh = do @ W2j
+    da = dh * b * silu_grad(a)
+    db = dh * silu(a)
+    return dict(dw1=da.T @ xe, dw3=db.T @ xe, dw2=do.T @ h)
 
 
 def rmsnorm_bf16(x, eps: float) -> np.ndarray:

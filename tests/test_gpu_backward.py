@@ -134,3 +134,40 @@ def test_backward_is_deterministic():
     b = run_backward(cfg, L, dy)
     for name in a:
         assert np.array_equal(a[name], b[name]), name
+
+
+def test_backward_full_dims_sampled():
+    # T=16384 at Mixtral dims (dim 4096, hidden 14336, top 2 of 8): ~4096 grouped
+    # rows per expert, so every GEMM runs many token tiles per expert and the dX
+    # GEMM walks each expert's rows in L2-sized blocks.  Checked: dx of sampled
+    # tokens, and the dW1 / dW3 rows and dW2 columns of sampled hidden units of
+    # three experts (each a sum over all of that expert's tokens).
+    moe = lib()
+    cfg = mi.CONFIGS["prefill"].replace(name="bwd-full", T=16384, seed=46310)
+    L = mi.make_layer(cfg)
+    filter_x(cfg, L.x, L.wg, L.shift)
+    dy = mi.gen_x(cfg.replace(seed=cfg.seed + 1))
+    n, d, h = cfg.n_experts, cfg.dim, cfg.hidden
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dx = torch.full((cfg.T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dwg = torch.full((d, n), float("nan"), **f32)
+    dw1 = torch.full((n, h, d), float("nan"), **f32)
+    dw3 = torch.full((n, h, d), float("nan"), **f32)
+    dw2 = torch.full((n, d, h), float("nan"), **f32)
+    ws = moe.new_backward_workspace(cfg)
+    moe.moe_layer_backward(cfg, dev_bf16(L.x), dev_bf16(L.wg), dev_bf16(L.w1), dev_bf16(L.w3),
+                           dev_bf16(L.w2), dev_bf16(dy), dx, dwg, dw1, dw3, dw2, ws)
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    rng = np.random.default_rng(cfg.seed)
+    rows = np.sort(rng.choice(cfg.T, 12, replace=False))
+    ref = orc.moe_layer_backward(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy[rows],
+                                 weight_grads=False)
+    got_dx = orc.widen_bf16(host_bits(dx[torch.as_tensor(rows, device="cuda")]))
+    close("dx (sampled tokens)", got_dx, ref["dx"], EXACT)
+    for e in (0, 3, 7):
+        units = np.sort(rng.choice(h, 3, replace=False))
+        r = orc.expert_weight_grad_units(L.x, L.wg, L.w1, L.w3, L.w2, cfg.top_k, dy, e, units)
+        u = torch.as_tensor(units, device="cuda")
+        close("dw1[%d] rows" % e, dw1[e][u].cpu().numpy(), r["dw1"], EXACT)
+        close("dw3[%d] rows" % e, dw3[e][u].cpu().numpy(), r["dw3"], EXACT)
+        close("dw2[%d] columns" % e, dw2[e][:, u].cpu().numpy(), r["dw2"], EXACT)

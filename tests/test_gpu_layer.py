@@ -139,3 +139,11 @@ def test_mixtral_8x22b_dims(path):
     # "Mixtral 8x22B, scaling the exact same architecture up": dim 6144, hidden 16384
     cfg = mi.Config("8x22b", T=48, dim=6144, hidden=16384, seed=46108)
     check_layer(cfg, path)
+
+
+def test_largest_batch_mixtral_dims_sampled():
+    # T = 65536 at Mixtral dims: T * K * hidden = 1.88e9, just under the 2^31
+    # limit of the supported shapes, so byte offsets into x_perm and H run far
+    # past 2^31 and every expert's rows are walked in L2-sized blocks
+    cfg = mi.CONFIGS["prefill"].replace(name="max-batch", T=65536, seed=46111)
+    check_layer(cfg, 0, sample=32)

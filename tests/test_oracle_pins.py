@@ -418,3 +418,25 @@ def test_backward_bf16_points_mode_stays_near_exact():
         rms = np.sqrt(np.mean(a[k] ** 2))
         assert np.max(np.abs(a[k] - b[k])) < 0.1 * rms, k
         assert np.max(np.abs(a[k] - b[k])) > 0, k
+
+
+def test_backward_unit_gradients_match_the_full_backward():
+    # the per-unit weight gradients (used to check large batches on sampled
+    # units) against the full backward, itself pinned by central differences
+    cfg = mi.Config("units", T=40, dim=16, hidden=24, n_experts=6, top_k=2, seed=4711)
+    L = mi.make_layer(cfg)
+    dy = mi.gen_x(cfg.replace(seed=4712))
+    full = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, 2, dy)
+    ids, _, _ = orc.router(L.x, L.wg, 2)
+    for e in range(cfg.n_experts):
+        units = [0, 5, 23] if e % 2 == 0 else [7, 11]
+        got = orc.expert_weight_grad_units(L.x, L.wg, L.w1, L.w3, L.w2, 2, dy, e, units)
+        scale = max(np.abs(full["dw1"]).max(), 1e-30)
+        assert np.allclose(got["dw1"], full["dw1"][e][units], rtol=1e-12, atol=1e-14 * scale)
+        assert np.allclose(got["dw3"], full["dw3"][e][units], rtol=1e-12, atol=1e-14 * scale)
+        assert np.allclose(got["dw2"], full["dw2"][e][:, units], rtol=1e-12, atol=1e-14 * scale)
+        if not np.any(ids == e):              # an expert with no tokens: zero gradients
+            assert not np.any(got["dw1"]) and not np.any(got["dw2"])
+    part = orc.moe_layer_backward(L.x, L.wg, L.w1, L.w3, L.w2, 2, dy, weight_grads=False)
+    assert part["dw1"] is None and part["dw2"] is None
+    assert np.array_equal(part["dx"], full["dx"]) and np.array_equal(part["dwg"], full["dwg"])
