@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the Mixtral sparse mixture-of-experts layer forward.
+"""fp64 CPU oracle of the Mixtral sparse mixture-of-experts layer: the forward,
+its backward with the routing held fixed, and the routing statistics.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import or run this module.
@@ -29,7 +30,15 @@ Readings where the pages are silent:
 * the routing structures are a stable counting sort of the flat assignments
   ``t*K + k`` by expert id (tokens ascending inside each expert group);
 * the 32-layer stack applies ``x <- x + MoE(RMSNorm(x))`` with unit gain and
-  eps = 1e-5, the normalised activations rounded to bf16 (not on the pages).
+  eps = 1e-5, the normalised activations rounded to bf16 (not on the pages);
+* the backward (the pages give no gradient) differentiates the layer output
+  with the expert selection held fixed -- TopK is piecewise constant -- so the
+  router weight and the input receive the gradient of the softmax over the
+  selected logits (``moe_layer_backward``, pinned by central differences);
+* the routing statistics (§5, Routing analysis: Fig. 7 and 9 expert shares,
+  Table 5 repeated consecutive assignments) are returned as counts:
+  per-(choice, expert) tokens, consecutive pairs with the same first choice
+  and consecutive pairs whose K chosen experts intersect.
 
 Precision: every input is widened exactly from bf16 to float64 and every step
 runs in float64.  ``h_bf16=True`` additionally rounds the SwiGLU activations to
