@@ -536,7 +536,11 @@ def run_backward_bench(args, rank, world):
                      "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
                      "traffic": None, "peak_kind": pk_kind + " sustained bf16",
                      "algorithmic_flop_per_step": flops},
-        "gpu_launches": args.steps * 21,
+        # per call: router, 4 grouping kernels (hist, scan, scatter, gather), the
+        # 2 forward GEMMs, combine / router / router-weight gradients, the dH and
+        # dX GEMMs, W_g transpose, input gradient, padding zeroes, 2 weight-
+        # gradient GEMMs
+        "gpu_launches": args.steps * 17,
         "clocks": clk,
     }
     if rank == 0:
