@@ -112,7 +112,19 @@ def _shape(shape) -> MoeShape:
 _BF16 = (torch.bfloat16, torch.uint16, torch.int16)
 
 
+def _need(*checks):
+    """Element counts, checked for every argument of a call before any pointer
+    is taken: each (tensor or None, elements the shape implies, name).  A
+    shorter tensor would let a kernel read or write past it."""
+    for t, numel, name in checks:
+        if isinstance(t, torch.Tensor) and t.numel() < numel:
+            raise ValueError("%s holds %d elements; the shape needs %d"
+                             % (name, t.numel(), numel))
+
+
 def _ptr(t, dtypes=None, name="tensor", nullable=False):
+    """Device pointer of a tensor after the checks the C ABI cannot make (type,
+    device, layout, dtype; element counts are _need's)."""
     if t is None:
         if nullable:
             return None
@@ -140,6 +152,13 @@ _I32 = (torch.int32,)
 _F32 = (torch.float32,)
 
 
+def _sizes(s):
+    """Element counts of every array of the boundary for shape s."""
+    T, d, h, n, K = s.T, s.dim, s.hidden, s.n_experts, s.top_k
+    R = T * K
+    return dict(x=T * d, wg=d * n, w=n * h * d, tk=R, n=n, off=n + 1, xp=R * d, hp=R * h)
+
+
 def moe_workspace_bytes(shape) -> int:
     s = _shape(shape)
     n = _LIB.moe_workspace_bytes(ctypes.byref(s))
@@ -163,17 +182,35 @@ def new_workspace(shape, device=None, stream=None) -> torch.Tensor:
 
 def moe_router_topk(shape, x, w_gate, ids, gates, counts, stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((x, z["x"], "x"),
+          (w_gate, z["wg"], "w_gate"),
+          (ids, z["tk"], "ids"),
+          (gates, z["tk"], "gates"),
+          (counts, z["n"], "counts"))
     _check(_LIB.moe_router_topk(ctypes.byref(s), _ptr(x, _BF16, "x"),
-                                _ptr(w_gate, _BF16, "w_gate"), _ptr(ids, _I32, "ids"),
-                                _ptr(gates, _F32, "gates"), _ptr(counts, _I32, "counts"),
+                                _ptr(w_gate, _BF16, "w_gate"),
+                                _ptr(ids, _I32, "ids"),
+                                _ptr(gates, _F32, "gates"),
+                                _ptr(counts, _I32, "counts"),
                                 _stream(stream)), "moe_router_topk")
 
 
 def moe_permute(shape, x, ids, offsets, perm_src, slot_row, x_perm, ws, stream=None) -> None:
     s = _shape(shape)
-    _check(_LIB.moe_permute(ctypes.byref(s), _ptr(x, _BF16, "x"), _ptr(ids, _I32, "ids"),
-                            _ptr(offsets, _I32, "offsets"), _ptr(perm_src, _I32, "perm_src"),
-                            _ptr(slot_row, _I32, "slot_row"), _ptr(x_perm, _BF16, "x_perm"),
+    z = _sizes(s)
+    _need((x, z["x"], "x"),
+          (ids, z["tk"], "ids"),
+          (offsets, z["off"], "offsets"),
+          (perm_src, z["tk"], "perm_src"),
+          (slot_row, z["tk"], "slot_row"),
+          (x_perm, z["xp"], "x_perm"))
+    _check(_LIB.moe_permute(ctypes.byref(s), _ptr(x, _BF16, "x"),
+                            _ptr(ids, _I32, "ids"),
+                            _ptr(offsets, _I32, "offsets"),
+                            _ptr(perm_src, _I32, "perm_src"),
+                            _ptr(slot_row, _I32, "slot_row"),
+                            _ptr(x_perm, _BF16, "x_perm"),
                             _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
                             _stream(stream)), "moe_permute")
 
@@ -181,17 +218,34 @@ def moe_permute(shape, x, ids, offsets, perm_src, slot_row, x_perm, ws, stream=N
 def moe_expert_ffn_grouped(shape, x_perm, offsets, w1, w3, w2, h, y_perm, ws,
                            path=MOE_FFN_AUTO, stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((x_perm, z["xp"], "x_perm"),
+          (offsets, z["off"], "offsets"),
+          (w1, z["w"], "w1"),
+          (w3, z["w"], "w3"),
+          (w2, z["w"], "w2"),
+          (h, z["hp"], "h"),
+          (y_perm, z["xp"], "y_perm"))
     _check(_LIB.moe_expert_ffn_grouped(
-        ctypes.byref(s), _ptr(x_perm, _BF16, "x_perm"), _ptr(offsets, _I32, "offsets"),
-        _ptr(w1, _BF16, "w1"), _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
-        _ptr(h, _BF16, "h"), _ptr(y_perm, _BF16, "y_perm"), int(path), _ptr(ws, name="ws"),
+        ctypes.byref(s), _ptr(x_perm, _BF16, "x_perm"),
+        _ptr(offsets, _I32, "offsets"),
+        _ptr(w1, _BF16, "w1"), _ptr(w3, _BF16, "w3"),
+        _ptr(w2, _BF16, "w2"), _ptr(h, _BF16, "h"),
+        _ptr(y_perm, _BF16, "y_perm"), int(path), _ptr(ws, name="ws"),
         ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn_grouped")
 
 
 def moe_combine(shape, y_perm, slot_row, gates, y, residual=None, stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((y_perm, z["xp"], "y_perm"),
+          (slot_row, z["tk"], "slot_row"),
+          (gates, z["tk"], "gates"),
+          (residual, z["x"], "residual"),
+          (y, z["x"], "y"))
     _check(_LIB.moe_combine(ctypes.byref(s), _ptr(y_perm, _BF16, "y_perm"),
-                            _ptr(slot_row, _I32, "slot_row"), _ptr(gates, _F32, "gates"),
+                            _ptr(slot_row, _I32, "slot_row"),
+                            _ptr(gates, _F32, "gates"),
                             _ptr(residual, _BF16, "residual", nullable=True),
                             _ptr(y, _BF16, "y"), _stream(stream)), "moe_combine")
 
@@ -215,17 +269,35 @@ def new_backward_workspace(shape, device=None, stream=None) -> torch.Tensor:
 def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, dx, dw_gate, dw1, dw3, dw2, ws,
                        stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((x, z["x"], "x"),
+          (w_gate, z["wg"], "w_gate"),
+          (w1, z["w"], "w1"),
+          (w3, z["w"], "w3"),
+          (w2, z["w"], "w2"),
+          (dy, z["x"], "dy"),
+          (dx, z["x"], "dx"),
+          (dw_gate, z["wg"], "dw_gate"),
+          (dw1, z["w"], "dw1"),
+          (dw3, z["w"], "dw3"),
+          (dw2, z["w"], "dw2"))
     _check(_LIB.moe_layer_backward(
-        ctypes.byref(s), _ptr(x, _BF16, "x"), _ptr(w_gate, _BF16, "w_gate"),
-        _ptr(w1, _BF16, "w1"), _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
-        _ptr(dy, _BF16, "dy"), _ptr(dx, _BF16, "dx"), _ptr(dw_gate, _F32, "dw_gate"),
-        _ptr(dw1, _F32, "dw1"), _ptr(dw3, _F32, "dw3"), _ptr(dw2, _F32, "dw2"),
+        ctypes.byref(s), _ptr(x, _BF16, "x"),
+        _ptr(w_gate, _BF16, "w_gate"), _ptr(w1, _BF16, "w1"),
+        _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
+        _ptr(dy, _BF16, "dy"), _ptr(dx, _BF16, "dx"),
+        _ptr(dw_gate, _F32, "dw_gate"), _ptr(dw1, _F32, "dw1"),
+        _ptr(dw3, _F32, "dw3"), _ptr(dw2, _F32, "dw2"),
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "moe_layer_backward")
 
 
 def moe_routing_stats(shape, ids, slot_counts, repeats, stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((ids, z["tk"], "ids"),
+          (slot_counts, s.top_k * s.n_experts, "slot_counts"),
+          (repeats, 2, "repeats"))
     _check(_LIB.moe_routing_stats(ctypes.byref(s), _ptr(ids, _I32, "ids"),
                                   _ptr(slot_counts, _I32, "slot_counts"),
                                   _ptr(repeats, _I32, "repeats"), _stream(stream)),
@@ -236,12 +308,24 @@ def moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, ids=None, gates=None,
                       rmsnorm_eps=None, residual=None, ffn_path=MOE_FFN_AUTO,
                       stream=None) -> None:
     s = _shape(shape)
+    z = _sizes(s)
+    _need((residual, z["x"], "residual"),
+          (x, z["x"], "x"),
+          (w_gate, z["wg"], "w_gate"),
+          (w1, z["w"], "w1"),
+          (w3, z["w"], "w3"),
+          (w2, z["w"], "w2"),
+          (y, z["x"], "y"),
+          (ids, z["tk"], "ids"),
+          (gates, z["tk"], "gates"))
     opts = MoeLayerOpts(1 if rmsnorm_eps is not None else 0,
                         float(rmsnorm_eps) if rmsnorm_eps is not None else 0.0,
-                        _ptr(residual, _BF16, "residual", nullable=True), int(ffn_path))
+                        _ptr(residual, _BF16, "residual", nullable=True),
+                        int(ffn_path))
     _check(_LIB.moe_layer_forward(
-        ctypes.byref(s), ctypes.byref(opts), _ptr(x, _BF16, "x"), _ptr(w_gate, _BF16, "w_gate"),
-        _ptr(w1, _BF16, "w1"), _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
+        ctypes.byref(s), ctypes.byref(opts), _ptr(x, _BF16, "x"),
+        _ptr(w_gate, _BF16, "w_gate"), _ptr(w1, _BF16, "w1"),
+        _ptr(w3, _BF16, "w3"), _ptr(w2, _BF16, "w2"),
         _ptr(y, _BF16, "y"), _ptr(ids, _I32, "ids", nullable=True),
         _ptr(gates, _F32, "gates", nullable=True), _ptr(ws, name="ws"),
         ws.numel() * ws.element_size(), _stream(stream)), "moe_layer_forward")
@@ -262,9 +346,18 @@ def moe_permute_noalloc(shape, x, ids, offsets, perm_src, slot_row, x_perm, stre
     """moe_permute for callers that cannot allocate a workspace: the library's
     own fixed device scratch is used instead (see include/moe.h)."""
     s = _shape(shape)
-    _check(_LIB.moe_permute_noalloc(ctypes.byref(s), _ptr(x, _BF16, "x"), _ptr(ids, _I32, "ids"),
+    z = _sizes(s)
+    _need((x, z["x"], "x"),
+          (ids, z["tk"], "ids"),
+          (offsets, z["off"], "offsets"),
+          (perm_src, z["tk"], "perm_src"),
+          (slot_row, z["tk"], "slot_row"),
+          (x_perm, z["xp"], "x_perm"))
+    _check(_LIB.moe_permute_noalloc(ctypes.byref(s), _ptr(x, _BF16, "x"),
+                                    _ptr(ids, _I32, "ids"),
                                     _ptr(offsets, _I32, "offsets"),
                                     _ptr(perm_src, _I32, "perm_src"),
                                     _ptr(slot_row, _I32, "slot_row"),
-                                    _ptr(x_perm, _BF16, "x_perm"), _stream(stream)),
+                                    _ptr(x_perm, _BF16, "x_perm"),
+                                    _stream(stream)),
            "moe_permute_noalloc")
