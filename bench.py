@@ -364,16 +364,22 @@ def oracle_sample(layers, prefill_tokens, decode_tokens=None, step=0):
 
 # ------------------------------------------------------------------ main ---
 
+def reference_sample_sizes(steps, warmup):
+    """Decode and prefill tokens the oracle evaluates per reference step: the
+    oracle takes ~0.15 s per token on 16 host threads, so about 720 tokens over
+    all K + W steps keeps the run near two minutes at any K (2 to 48 per step,
+    a third of them from the decode batch)."""
+    per_step = max(2, min(48, 720 // max(1, steps + warmup)))
+    decode_tokens = max(1, per_step // 3)
+    return decode_tokens, per_step - decode_tokens
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     metric, dec_name, pre_name = WORKLOADS[args.workload]
     layers = {DECODE: load_layer(dec_name), PREFILL: load_layer(pre_name)}
-    # the oracle takes ~0.15 s per token on 16 host threads: about 720 tokens
-    # over all K + W steps keeps the run near two minutes at any K
-    per_step = max(2, min(48, 720 // max(1, args.steps + args.warmup)))
-    decode_tokens = max(1, per_step // 3)
-    prefill_tokens = per_step - decode_tokens
+    decode_tokens, prefill_tokens = reference_sample_sizes(args.steps, args.warmup)
     for i in range(args.warmup):
         oracle_sample(layers, prefill_tokens, decode_tokens, step=i)
     total_tok, total_s = 0, 0.0
