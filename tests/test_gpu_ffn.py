@@ -191,3 +191,11 @@ def test_stream_k_counters_return_to_zero():
     assert_bf16_close(outs[0][1], ref_y, "expert outputs")
     for h, y in outs[1:]:
         assert np.array_equal(h, outs[0][0]) and np.array_equal(y, outs[0][1])
+
+
+def test_stream_whole_tile_schedule_beyond_the_stream_k_counters():
+    # 256 experts of hidden 8192: a pass can have (R/32 + n) * 64 = 24832 tiles,
+    # more than the stream-K arrival counters hold, so the weight stream runs
+    # its whole-tile schedule (ragged groups of 0 to 33 rows)
+    counts = [[0, 1, 2, 31, 32, 33][e % 6] for e in range(256)]
+    check_ffn(counts, 128, 8192, "stream", seed=23)
