@@ -4,19 +4,28 @@ A step is one pass of the whole hot path over two batches of synthetic
 Mixtral-shaped tokens (dim 4096, hidden 14336, 8 experts, top-2; Table 1 of
 "Mixtral of Experts"): a decode-sized layer call (T=16, weight-bandwidth
 bound, small-T weight-stream FFN) and a prefill-sized layer call (T=4096,
-tensor-core bound, grouped-GEMM FFN), each router -> grouping -> expert FFN ->
-combine through the C ABI on resident inputs.  value = tokens of both batches
-per second of step time.  Per-layer figures and the roofline of the dominant
-unit (the prefill expert FFN: its two tcgen05 grouped-GEMM kernels) are
-reported beside it, as is the fp64 oracle timed on the host cores.
+tensor-core bound, CTA-pair grouped-GEMM FFN), each one moe_layer_forward call
+(router -> grouping -> expert FFN -> combine) through the C ABI on resident
+inputs.  value = tokens of both batches per second of step time.
+
+Beside it: per-layer times; a per-phase breakdown (router + grouping, expert
+FFN, combine) from a second loop of the step-by-step entry points, which also
+times the dominant unit for the roofline (the prefill expert FFN: its two
+tcgen05 grouped-GEMM kernels); the end-to-end rate with host copies; the
+fp64 oracle timed on the host cores; and a parity check of the timed build's
+outputs against that oracle on the tokens it evaluated (the run fails if
+they disagree).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mixtral|fine]
+                    [--workload mixtral|fine|skew|stack|backward]
 
---workload fine times the same step on the fine-grained variant the pages
-mention (top 8 of 160 smaller experts, expert hidden 1792) instead of Mixtral.
---workload backward times moe_layer_backward (forward recompute + all
-gradients) on the Mixtral prefill batch (T=4096).
+--workload fine: the same step on the fine-grained variant the pages mention
+(top 8 of 160 smaller experts, expert hidden 1792).  --workload skew: one
+layer call on T=16384 tokens whose top-1 choices follow Zipf(1.2) over the
+experts.  --workload stack: the residual stack x <- x + MoE_l(RMSNorm(x)) over
+32 layers with independent weights, T=8192.  --workload backward:
+moe_layer_backward (forward recompute + all gradients) on the Mixtral prefill
+batch.
 
 Under torchrun (N > 1) every rank runs an independent replica (the layer has
 no cross-GPU exchange here); timing is max over ranks.
@@ -24,6 +33,7 @@ no cross-GPU exchange here); timing is max over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -38,28 +48,38 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s at Mixtral dims (T=16/4096) + % of TC/HBM roofline"
-DECODE, PREFILL = "decode", "prefill"
-# workload -> (metric, configuration of the decode-sized call, of the prefill-sized call)
+DECODE, PREFILL, SKEW = "decode", "prefill", "skew"
+# workload -> metric and the layer calls of one step: (role, input configuration)
 WORKLOADS = {
-    "mixtral": (METRIC, "decode", "prefill"),
-    "fine": ("MoE-layer tokens/s, fine-grained 160 experts top-8 (T=16/4096) "
-             "+ % of TC/HBM roofline", "fine_decode", "fine"),
+    "mixtral": dict(metric=METRIC, layers=((DECODE, "decode"), (PREFILL, "prefill"))),
+    "fine": dict(metric="MoE-layer tokens/s, fine-grained 160 experts top-8 (T=16/4096) "
+                        "+ % of TC/HBM roofline",
+                 layers=((DECODE, "fine_decode"), (PREFILL, "fine"))),
+    "skew": dict(metric="MoE-layer tokens/s, Zipf(1.2)-skewed routing (T=16384, Mixtral dims) "
+                        "+ % of TC roofline",
+                 layers=((SKEW, "skew"),)),
 }
+STACK_METRIC = ("MoE-stack tokens/s, 32 residual layers x <- x + MoE(RMSNorm(x)) "
+                "(T=8192, Mixtral dims) + % of TC roofline")
+# spec tolerance of every bf16 output: |gpu - oracle| <= ATOL + RTOL |oracle|
+ATOL, RTOL = 1e-2, 1e-2
+MIN_GAP_SELECT = 1e-2   # a token's selection is decided when its K-th / (K+1)-th logit gap is >= this
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["backward"], default="mixtral")
-    p.add_argument("--profile", choices=[DECODE, PREFILL, "skew", "fine_decode", "fine",
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["stack", "backward"],
+                   default="mixtral")
+    p.add_argument("--profile", choices=[DECODE, PREFILL, SKEW, "fine_decode", "fine",
                                          "backward"],
                    default=None,
                    help="no timing: run W warm-up + K layer calls of one workload (for ncu)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def dist_setup(ngpu):
@@ -117,10 +137,16 @@ def alg_flops(cfg):
     return cfg.T * (2 * cfg.dim * cfg.n_experts + cfg.top_k * 6 * cfg.dim * cfg.hidden)
 
 
-def alg_bytes(cfg, touched):
-    """Algorithmic HBM bytes: touched experts' weights + router + x in + y out."""
+def alg_bytes(cfg, touched, residual=False):
+    """Algorithmic HBM bytes: touched experts' weights + router + x in + y out
+    (+ the residual read of the stack workload)."""
     return (touched * 3 * cfg.dim * cfg.hidden * 2 + cfg.dim * cfg.n_experts * 2
-            + 2 * cfg.T * cfg.dim * 2)
+            + (3 if residual else 2) * cfg.T * cfg.dim * 2)
+
+
+def ffn_flops(cfg):
+    """FLOPs of the two grouped GEMMs of one expert-FFN call: 6 d h per grouped row."""
+    return 6.0 * cfg.T * cfg.top_k * cfg.dim * cfg.hidden
 
 
 class Buffers:
@@ -148,6 +174,12 @@ class Buffers:
         self.ws = moe.new_workspace(cfg)
         self.x_host = torch.from_numpy(np.ascontiguousarray(L.x).view(np.int16)).view(
             torch.bfloat16).pin_memory()
+
+    def forward(self, stream=None):
+        """The whole layer, one C-ABI call (what a user calls)."""
+        import sparse_mixture_experts_46_b300 as moe
+        moe.moe_layer_forward(self.cfg, self.x, self.wg, self.w1, self.w3, self.w2, self.y,
+                              self.ws, ids=self.ids, gates=self.gates, stream=stream)
 
     def router_permute(self):
         import sparse_mixture_experts_46_b300 as moe
@@ -219,8 +251,9 @@ class E2E:
                     self.compute.wait_event(s["down"])
 
 
-# kernels of YOUR launches per layer call: router, grouping (3 kernels above 2048 assignments,
-# 1 below), gather, gate/up GEMM, down GEMM, combine
+# Kernels of ours launched per layer call (moe_layer_forward): router, grouping
+# (one kernel up to 2048 assignments, histogram / scan / scatter above), gather,
+# gate/up GEMM, down GEMM, combine.
 def kernels_per_layer(cfg):
     return 1 + (3 if cfg.T * cfg.top_k > 2048 else 1) + 1 + 2 + 1
 
@@ -228,7 +261,8 @@ def kernels_per_layer(cfg):
 # --------------------------------------------------------------- clocks ---
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples; only those inside the timed window count."""
+    """nvidia-smi clock / throttle samples every 20 ms; statistics are taken
+    over the samples inside each named wall-clock window."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -237,45 +271,55 @@ class ClockSampler:
     def __init__(self):
         import torch
         self.proc = None
-        self.window = None
+        self.windows = {}
+        self.rows = None
         try:
             uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
             ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", ident, "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, AttributeError):
             self.proc = None
         time.sleep(0.5)  # let nvidia-smi start sampling before the timed region
 
-    def mark(self, t0, t1):
-        """Wall-clock bounds (datetime) of the timed region."""
-        self.window = (t0, t1)
+    def mark(self, t0, t1, name="timed"):
+        """Wall-clock bounds (datetime) of a timed region."""
+        self.windows[name] = (t0, t1)
 
-    def stop(self):
+    def _collect(self):
+        if self.rows is not None:
+            return self.rows
+        self.rows = []
         if self.proc is None:
-            return None
+            return self.rows
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        import datetime
-        rows = []
         for line in out.splitlines():
             f = [v.strip() for v in line.split(",")]
             if len(f) < 9:
                 continue
             try:
                 ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
-                rows.append((ts, float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+                self.rows.append((ts, float(f[1]), float(f[2]), float(f[3]), f[5:9]))
             except ValueError:
                 continue
-        if self.window is not None:
-            lo = self.window[0] - datetime.timedelta(seconds=0.05)
-            hi = self.window[1] + datetime.timedelta(seconds=0.05)
+        return self.rows
+
+    def stop(self, name="timed"):
+        """Clock record of window `name` (all samples when it was never marked)."""
+        rows = self._collect()
+        if self.proc is None and not rows:
+            return None
+        win = self.windows.get(name)
+        if win is not None:
+            lo = win[0] - datetime.timedelta(seconds=0.05)
+            hi = win[1] + datetime.timedelta(seconds=0.05)
             inside = [r for r in rows if lo <= r[0] <= hi]
         else:
             inside = rows
@@ -332,6 +376,36 @@ def peaks():
             "fallback"
 
 
+def tensor_peak(pk, clk):
+    """The bf16 tensor peak that applies to a kernel timed under the clock
+    record `clk`: the burst figure when the median SM clock under load was
+    within 5 % of the maximum (the power cap had not pulled it down), the
+    sustained figure otherwise.  No record: burst (the smaller fraction)."""
+    mhz = clk.get("sm_mhz") if clk else None
+    top = clk.get("sm_max_mhz") if clk else None
+    if mhz is None or top is None or mhz >= 0.95 * top:
+        return pk["bf16_tflops"], "burst"
+    return pk["bf16_tflops_sustained"], "sustained"
+
+
+def ffn_roofline(ffn, pk, pk_kind, traffic, clk=None):
+    """Roofline of an expert-FFN call against whichever peak binds it: the bf16
+    tensor rate (Mixtral: 2.9 TFLOP on 2.8 GB per prefill call) or the HBM copy
+    bandwidth (fine-grained experts: 7 GB of weights for half the FLOPs).  The
+    tensor peak is burst or sustained by the clocks seen (tensor_peak)."""
+    p_tc, which = tensor_peak(pk, clk)
+    t_tc = ffn["ffn_tflops"] / p_tc
+    t_hbm = ffn["ffn_hbm_gbs"] / pk["hbm_gbs"]
+    if t_tc >= t_hbm:
+        return {"bound": "tensor", "achieved": ffn["ffn_tflops"], "peak": p_tc,
+                "unit": "TFLOP/s", "frac": t_tc, "traffic": traffic,
+                "peak_kind": "%s %s bf16 (cuBLAS)" % (pk_kind, which),
+                "frac_of_burst": ffn["ffn_tflops"] / pk["bf16_tflops"],
+                "frac_of_sustained": ffn["ffn_tflops"] / pk["bf16_tflops_sustained"]}
+    return {"bound": "hbm", "achieved": ffn["ffn_hbm_gbs"], "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": t_hbm, "traffic": traffic, "peak_kind": pk_kind + " copy"}
+
+
 # ------------------------------------------------------------ oracle CPU ---
 
 def cpu_cores():
@@ -343,56 +417,105 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(layers, prefill_tokens, decode_tokens=None, step=0):
-    """The oracle on a sample of the step's tokens: `decode_tokens` of the decode
-    batch (all of it when None) and `prefill_tokens` of the prefill batch, taken
-    from fixed seeded permutations of each batch, the window moving with `step`."""
+def sample_rows(T, k, seed, step=0):
+    """k rows of a T-token batch from a fixed seeded permutation, the window moving with `step`."""
+    k = min(k, T)
+    perm = np.random.default_rng(seed).permutation(T)
+    return np.sort(perm[(step * k + np.arange(k)) % T])
+
+
+def oracle_sample(layers, counts, step=0):
+    """The oracle on a sample of each layer's tokens: counts[role] tokens
+    (all of them when None) from a fixed seeded permutation of that batch.
+    Returns (tokens, seconds, {role: (rows, y_ref, ids_ref, logits)})."""
     from oracle import moe_oracle as orc
-    tokens = 0
-    t0 = time.perf_counter()
-    for name, (cfg, L) in layers.items():
-        k = (cfg.T if decode_tokens is None else decode_tokens) if name == DECODE else prefill_tokens
-        k = min(k, cfg.T)
+    tokens, secs, out = 0, 0.0, {}
+    for i, (role, (cfg, L)) in enumerate(layers.items()):
+        k = counts.get(role)
+        k = cfg.T if k is None else min(k, cfg.T)
         if k <= 0:
             continue
-        perm = np.random.default_rng(1 if name != DECODE else 2).permutation(cfg.T)
-        rows = np.sort(perm[(step * k + np.arange(k)) % cfg.T])
-        orc.moe_layer(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k)
+        rows = sample_rows(cfg.T, k, 1 + i, step)
+        t0 = time.perf_counter()
+        y, ids, _ = orc.moe_layer(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k)
+        secs += time.perf_counter() - t0
         tokens += len(rows)
-    return tokens, time.perf_counter() - t0
+        out[role] = (rows, y, ids, orc.router_logits(L.x[rows], L.wg))
+    return tokens, secs, out
 
 
-# ------------------------------------------------------------------ main ---
+def parity_check(got_y, got_ids, ref_y, ref_ids, logits, top_k):
+    """North-star parity of sampled tokens: selected experts equal the
+    oracle's wherever the selection is decided (K-th / (K+1)-th logit gap >=
+    1e-2), every output element of a token routed like the oracle within
+    1e-2 + 1e-2 |oracle|.  got_y: float64 [k, dim]; returns a summary dict."""
+    srt = -np.sort(-logits, axis=1)
+    decided = (srt[:, top_k - 1] - srt[:, top_k] >= MIN_GAP_SELECT) if top_k < srt.shape[1] \
+        else np.ones(len(srt), dtype=bool)
+    same = np.all(np.sort(got_ids, axis=1) == np.sort(ref_ids, axis=1), axis=1)
+    routing_ok = bool(np.all(same[decided]))
+    err = np.abs(got_y[same] - ref_y[same])
+    ratio = err / (ATOL + RTOL * np.abs(ref_y[same])) if err.size else np.zeros(1)
+    return {"tokens": int(len(ref_y)), "compared": int(same.sum()),
+            "undecided_routing": int((~decided).sum()),
+            "max_abs_err": float(err.max()) if err.size else 0.0,
+            "max_err_over_bound": float(ratio.max()),
+            "ok": bool(routing_ok and np.all(ratio <= 1.0) and np.all(np.isfinite(got_y)))}
+
+
+def merge_parity(parts):
+    parts = [p for p in parts if p is not None]
+    if not parts:
+        return None
+    return {"tokens": sum(p["tokens"] for p in parts),
+            "compared": sum(p["compared"] for p in parts),
+            "undecided_routing": sum(p["undecided_routing"] for p in parts),
+            "max_abs_err": max(p["max_abs_err"] for p in parts),
+            "max_err_over_bound": max(p["max_err_over_bound"] for p in parts),
+            "tolerance": "|gpu - oracle| <= 1e-2 + 1e-2 |oracle|",
+            "ok": all(p["ok"] for p in parts)}
+
+
+# ------------------------------------------------------------ reference ---
 
 def reference_sample_sizes(steps, warmup):
-    """Decode and prefill tokens the oracle evaluates per reference step: the
-    oracle takes ~0.15 s per token on 16 host threads, so about 720 tokens over
-    all K + W steps keeps the run near two minutes at any K (2 to 48 per step,
-    a third of them from the decode batch)."""
+    """Tokens the oracle evaluates per reference step (first / second layer of
+    the step): the oracle takes ~0.15 s per Mixtral token on 16 host threads,
+    so about 720 tokens over all K + W steps keeps the run near two minutes at
+    any K (2 to 48 per step, a third of them from the first layer's batch)."""
     per_step = max(2, min(48, 720 // max(1, steps + warmup)))
-    decode_tokens = max(1, per_step // 3)
-    return decode_tokens, per_step - decode_tokens
+    first = max(1, per_step // 3)
+    return first, per_step - first
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    metric, dec_name, pre_name = WORKLOADS[args.workload]
-    layers = {DECODE: load_layer(dec_name), PREFILL: load_layer(pre_name)}
-    decode_tokens, prefill_tokens = reference_sample_sizes(args.steps, args.warmup)
+    if args.workload in ("stack", "backward"):
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the oracle reference arm times the forward layer workloads "
+                          "(mixtral, fine, skew) only"}), flush=True)
+        return
+    wl = WORKLOADS[args.workload]
+    layers = {role: load_layer(name) for role, name in wl["layers"]}
+    first, second = reference_sample_sizes(args.steps, args.warmup)
+    roles = list(layers)
+    counts = {roles[0]: first if len(roles) > 1 else first + second}
+    if len(roles) > 1:
+        counts[roles[1]] = second
     for i in range(args.warmup):
-        oracle_sample(layers, prefill_tokens, decode_tokens, step=i)
+        oracle_sample(layers, counts, step=i)
     total_tok, total_s = 0, 0.0
     for i in range(args.steps):
-        tok, s = oracle_sample(layers, prefill_tokens, decode_tokens, step=args.warmup + i)
+        tok, s, _ = oracle_sample(layers, counts, step=args.warmup + i)
         total_tok += tok
         total_s += s
     value = total_tok / total_s
-    sample = ("fp64 oracle per step: %d decode + %d prefill tokens of the step's batches "
-              "(seeded windows moving each step; %d tokens over the %d steps)"
-              % (decode_tokens, prefill_tokens, total_tok, args.steps))
+    sample = ("fp64 oracle per step: %s tokens of the step's batches (seeded windows moving "
+              "each step; %d tokens over the %d steps)"
+              % (" + ".join("%d %s" % (counts[r], r) for r in roles), total_tok, args.steps))
     print(json.dumps({
-        "impl": "reference", "metric": metric, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": wl["metric"], "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -403,6 +526,8 @@ def run_reference(args, rank, world):
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
+
+# -------------------------------------------------------------- profile ---
 
 def run_profile_backward(args):
     """W + K moe_layer_backward calls on a reduced case for section captures:
@@ -442,7 +567,7 @@ def run_profile_case(args):
     cfg, L = load_layer(args.profile)
     b = Buffers(cfg, L)
     for _ in range(args.warmup + args.steps):
-        moe.moe_layer_forward(cfg, b.x, b.wg, b.w1, b.w3, b.w2, b.y, b.ws)
+        b.forward()
     torch.cuda.synchronize()
     st = moe.moe_check_error(b.ws)
     if st != moe.MOE_OK:
@@ -451,36 +576,28 @@ def run_profile_case(args):
 
 
 def config_block(layers):
-    dc = layers[DECODE][0]
-    pc = layers[PREFILL][0]
-    gb = pc.n_experts * 3 * pc.dim * pc.hidden * 2 / 1e9
-    if dc.n_experts == 8:
-        what = ("Mixtral-shaped MoE layer, decode batch T=16 + prefill batch T=4096 "
-                "(dim 4096, hidden 14336, 8 experts, top-2, bf16 weights)")
+    cfgs = [c for c, _ in layers.values()]
+    c0 = cfgs[-1]
+    gb = c0.n_experts * 3 * c0.dim * c0.hidden * 2 / 1e9
+    Ts = [c.T for c in cfgs]
+    if c0.zipf_s > 0:
+        what = ("Mixtral-shaped MoE layer, T=%d tokens with Zipf(%.1f)-skewed top-1 routing "
+                "(dim %d, hidden %d, %d experts, top-%d, bf16 weights)"
+                % (c0.T, c0.zipf_s, c0.dim, c0.hidden, c0.n_experts, c0.top_k))
+    elif c0.n_experts == 8:
+        what = ("Mixtral-shaped MoE layer, decode batch T=%d + prefill batch T=%d "
+                "(dim 4096, hidden 14336, 8 experts, top-2, bf16 weights)" % tuple(Ts))
     else:
         what = ("fine-grained MoE layer, decode batch T=%d + prefill batch T=%d (dim %d, "
                 "hidden %d, %d experts, top-%d, bf16 weights)"
-                % (dc.T, pc.T, pc.dim, pc.hidden, pc.n_experts, pc.top_k))
-    return {"workload": what,
-            "T": [layers[DECODE][0].T, layers[PREFILL][0].T], "dim": dc.dim,
-            "hidden": dc.hidden, "n_experts": dc.n_experts, "top_k": dc.top_k,
-            "parallelism": "replicas", "l2": "inputs larger than L2 (%.1f GB of expert "
-                                             "weights per layer, streamed every step)" % gb}
+                % (Ts[0], Ts[-1], c0.dim, c0.hidden, c0.n_experts, c0.top_k))
+    return {"workload": what, "T": Ts, "dim": c0.dim, "hidden": c0.hidden,
+            "n_experts": c0.n_experts, "top_k": c0.top_k, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (%.1f GB of expert weights per layer, streamed "
+                  "every step)" % gb}
 
 
-def ffn_roofline(pre, pk, pk_kind, traffic):
-    """Roofline of the prefill expert FFN against whichever peak binds it: the
-    sustained bf16 tensor rate (Mixtral, 2.9 TFLOP on 2.8 GB) or the HBM copy
-    bandwidth (fine-grained experts: 7 GB of weights for half the FLOPs)."""
-    t_tc = pre["ffn_tflops"] / pk["bf16_tflops_sustained"]
-    t_hbm = pre["ffn_hbm_gbs"] / pk["hbm_gbs"]
-    if t_tc >= t_hbm:
-        return {"bound": "tensor", "achieved": pre["ffn_tflops"],
-                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": t_tc,
-                "traffic": traffic, "peak_kind": pk_kind + " sustained bf16 (cuBLAS, 4 s loop)"}
-    return {"bound": "hbm", "achieved": pre["ffn_hbm_gbs"], "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": t_hbm, "traffic": traffic, "peak_kind": pk_kind + " copy"}
-
+# ------------------------------------------------------------- backward ---
 
 def run_backward_bench(args, rank, world):
     """The layer backward on the prefill batch: one step = one moe_layer_backward
@@ -512,7 +629,6 @@ def run_backward_bench(args, rank, world):
     clocks = ClockSampler()
     barrier(world)
     torch.cuda.synchronize()
-    import datetime
     w0 = datetime.datetime.now()
     start.record()
     for _ in range(args.steps):
@@ -527,6 +643,7 @@ def run_backward_bench(args, rank, world):
     R = T * K
     flops = 18.0 * R * d * h + 2 * T * d * n * 3   # forward (6Rdh) + backward GEMMs (12Rdh) + router
     pk, pk_kind = peaks()
+    p_tc, which = tensor_peak(pk, clk)
     tflops = flops / (ms * 1e-3) / 1e12
     result = {
         "metric": "MoE-layer backward tokens/s at Mixtral dims (T=4096) + % of TC roofline",
@@ -538,9 +655,11 @@ def run_backward_bench(args, rank, world):
                                "dW1, dW3, dW2), T=4096, dim 4096, hidden 14336, 8 experts, top-2",
                    "T": T, "dim": d, "hidden": h, "n_experts": n, "top_k": K,
                    "parallelism": "replicas"},
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops_sustained"],
-                     "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
-                     "traffic": None, "peak_kind": pk_kind + " sustained bf16",
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": p_tc,
+                     "unit": "TFLOP/s", "frac": tflops / p_tc,
+                     "traffic": None, "peak_kind": "%s %s bf16" % (pk_kind, which),
+                     "frac_of_burst": tflops / pk["bf16_tflops"],
+                     "frac_of_sustained": tflops / pk["bf16_tflops_sustained"],
                      "algorithmic_flop_per_step": flops},
         # per call: router, 4 grouping kernels (hist, scan, scatter, gather), the
         # 2 forward GEMMs, combine / router / router-weight gradients, the dH and
@@ -553,106 +672,240 @@ def run_backward_bench(args, rank, world):
         print(json.dumps(result), flush=True)
 
 
-def main():
-    args = parse()
-    rank, world = dist_setup(args.gpus)
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
+# ---------------------------------------------------------------- stack ---
 
+def run_stack_bench(args, rank, world):
+    """The residual stack x <- x + MoE_l(RMSNorm(x)) over 32 layers with
+    independent weights (90 GB resident), T=8192: one step = 32
+    moe_layer_forward calls.  value = tokens through the whole stack per
+    second.  The oracle checks the timed build layer by layer (teacher-forced:
+    each layer takes the GPU's bf16 input) on a few sampled tokens, and its
+    time is the CPU baseline."""
     import torch
     import sparse_mixture_experts_46_b300 as moe
-    if args.profile is not None:
-        run_profile_case(args)
-        return
-    if args.workload == "backward":
-        run_backward_bench(args, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-    metric, dec_name, pre_name = WORKLOADS[args.workload]
-    layers = {DECODE: load_layer(dec_name), PREFILL: load_layer(pre_name)}
-    bufs = {k: Buffers(cfg, L) for k, (cfg, L) in layers.items()}
+    import moe_inputs as mi
+    cfg = mi.CONFIGS["stack"]
+    T, d, n, K, NL = cfg.T, cfg.dim, cfg.n_experts, cfg.top_k, cfg.layers
+    x0 = to_dev(mi.gen_x(cfg))
+    weights = []
+    for layer in range(NL):
+        wg = mi.gen_router_weight(cfg, layer)
+        w1, w3, w2 = mi.gen_experts(cfg, layer)
+        weights.append(tuple(to_dev(a) for a in (wg, w1, w3, w2)))
+        del w1, w3, w2
+    bufs = [torch.empty_like(x0), torch.empty_like(x0)]
+    ids = [torch.empty((T, K), dtype=torch.int32, device="cuda") for _ in range(NL)]
+    ws = moe.new_workspace(cfg)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        for i, name in enumerate((DECODE, PREFILL)):
-            b = bufs[name]
-            if ev is not None:
-                ev[name][0].record(stream)
-            b.router_permute()
-            if ev is not None:
-                ev[name][1].record(stream)
-            b.ffn()
-            if ev is not None:
-                ev[name][2].record(stream)
-            b.combine()
-            if ev is not None:
-                ev[name][3].record(stream)
+    def step(ev=None, keep=None):
+        cur = x0
+        for layer, (wg, w1, w3, w2) in enumerate(weights):
+            y = bufs[layer & 1] if keep is None else keep[layer]
+            moe.moe_layer_forward(cfg, cur, wg, w1, w3, w2, y, ws, ids=ids[layer],
+                                  rmsnorm_eps=cfg.rmsnorm_eps, residual=cur)
+            cur = y
+        if ev is not None:
+            ev.record(stream)
+        return cur
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    for b in bufs.values():
-        st = moe.moe_check_error(b.ws)
-        if st != moe.MOE_OK:
-            raise RuntimeError("device error word after warm-up: %d" % st)
-
+    if moe.moe_check_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device error word after warm-up")
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    evs = [{n: [mk() for _ in range(4)] for n in (DECODE, PREFILL)} for _ in range(args.steps)]
-    start, end = mk(), mk()
+    start = mk()
+    ends = [mk() for _ in range(args.steps)]
     clocks = ClockSampler()
     barrier(world)
     torch.cuda.synchronize()
-    import datetime
     w0 = datetime.datetime.now()
     start.record(stream)
     for k in range(args.steps):
-        step(evs[k])
-    end.record(stream)
+        step(ends[k])
     torch.cuda.synchronize()
     w1 = datetime.datetime.now()
     barrier(world)
     clocks.mark(w0, w1)
     clk = clocks.stop()
-    ms_total = max_over_ranks(start.elapsed_time(end), world)
+    ms_step = max_over_ranks(start.elapsed_time(ends[-1]), world) / args.steps
+    if moe.moe_check_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device error word after timing")
+
+    pk, pk_kind = peaks()
+    p_tc, which = tensor_peak(pk, clk)
+    layer_ms = ms_step / NL
+    layer_tflops = alg_flops(cfg) / (layer_ms * 1e-3) / 1e12
+    result = {
+        "metric": STACK_METRIC, "value": job_tokens_per_s(T, world, ms_step), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator, Table 1 shapes, independent random-init weights "
+                "per layer)",
+        "config": {"workload": "32-layer residual MoE stack x <- x + MoE_l(RMSNorm(x)), T=8192 "
+                               "(dim 4096, hidden 14336, 8 experts, top-2, bf16 weights, 90 GB)",
+                   "T": T, "dim": d, "hidden": cfg.hidden, "n_experts": n, "top_k": K,
+                   "layers": NL, "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (90 GB of weights streamed every step)"},
+        "layer_ms": layer_ms, "layer_tokens_per_s": T / (layer_ms * 1e-3),
+        # the stack has no step-by-step entry point for its RMSNorm router, so
+        # the unit here is one whole residual layer
+        "roofline": {"bound": "tensor", "achieved": layer_tflops, "peak": p_tc,
+                     "unit": "TFLOP/s", "frac": layer_tflops / p_tc, "traffic": None,
+                     "peak_kind": "%s %s bf16 (cuBLAS)" % (pk_kind, which),
+                     "kernel": "one residual layer (RMSNorm router, grouping, expert FFN, "
+                               "combine with residual)",
+                     "algorithmic_flop_per_layer": alg_flops(cfg)},
+        "gpu_launches": args.steps * NL * kernels_per_layer(cfg),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import moe_oracle as orc
+        rows = sample_rows(T, 4, 5)
+        keep = [torch.empty_like(x0) for _ in range(NL)]
+        step(keep=keep)
+        torch.cuda.synchronize()
+        host = [x0[torch.as_tensor(rows, device="cuda")]] + \
+               [k[torch.as_tensor(rows, device="cuda")] for k in keep]
+        host = [h.view(torch.int16).cpu().numpy().view(np.uint16) for h in host]
+        got_ids = [i[torch.as_tensor(rows, device="cuda")].cpu().numpy() for i in ids]
+        del keep
+        secs = 0.0
+        parts = []
+        for layer in range(NL):
+            wg = mi.gen_router_weight(cfg, layer)
+            w1, w3, w2 = mi.gen_experts(cfg, layer)
+            t0 = time.perf_counter()
+            ref, r_ids, _, u = orc.stack_layer(host[layer], wg, w1, w3, w2, K, cfg.rmsnorm_eps)
+            secs += time.perf_counter() - t0
+            parts.append(parity_check(orc.widen_bf16(host[layer + 1]), got_ids[layer], ref,
+                                      r_ids, orc.router_logits(u, wg), K))
+        result["cpu_baseline"] = {
+            "value": len(rows) / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "fp64 oracle: %d seeded tokens through all %d layers, each layer "
+                      "teacher-forced on the GPU's bf16 input, %.1f s" % (len(rows), NL, secs)}
+        result["parity"] = merge_parity(parts)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if result.get("parity") is not None and not result["parity"]["ok"]:
+        raise SystemExit("parity check against the oracle failed")
+
+
+# ---------------------------------------------------------------- layers ---
+
+def run_layers_bench(args, rank, world):
+    import torch
+    import sparse_mixture_experts_46_b300 as moe
+    wl = WORKLOADS[args.workload]
+    layers = {role: load_layer(name) for role, name in wl["layers"]}
+    roles = list(layers)
+    main_role = roles[-1]                     # the tensor-bound batch: its FFN is the roofline unit
+    bufs = {r: Buffers(cfg, L) for r, (cfg, L) in layers.items()}
+    stream = torch.cuda.current_stream()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def fused_step(ev=None):
+        for r in roles:
+            bufs[r].forward()
+            if ev is not None:
+                ev[r].record(stream)
+
+    def phased_step(ev):
+        for r in roles:
+            b = bufs[r]
+            ev[r][0].record(stream)
+            b.router_permute()
+            ev[r][1].record(stream)
+            b.ffn()
+            ev[r][2].record(stream)
+            b.combine()
+            ev[r][3].record(stream)
+
+    def check_device(when):
+        for b in bufs.values():
+            st = moe.moe_check_error(b.ws)
+            if st != moe.MOE_OK:
+                raise RuntimeError("device error word %s: %d" % (when, st))
+
+    for _ in range(args.warmup):
+        fused_step()
+    torch.cuda.synchronize()
+    check_device("after warm-up")
+
+    # (A) the timed region: the step through moe_layer_forward, one event per layer
+    clocks = ClockSampler()
+    evs = [{r: mk() for r in roles} for _ in range(args.steps)]
+    start = mk()
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = datetime.datetime.now()
+    start.record(stream)
+    for k in range(args.steps):
+        fused_step(evs[k])
+    torch.cuda.synchronize()
+    w1 = datetime.datetime.now()
+    barrier(world)
+    clocks.mark(w0, w1, "timed")
+    ms_total = max_over_ranks(start.elapsed_time(evs[-1][roles[-1]]), world)
     ms_step = ms_total / args.steps
 
-    def mean_ms(name, a, b):
-        return statistics.fmean(e[name][a].elapsed_time(e[name][b]) for e in evs)
+    def layer_ms(r):
+        i = roles.index(r)
+        vals = []
+        for k in range(args.steps):
+            if i > 0:
+                a = evs[k][roles[i - 1]]
+            else:
+                a = evs[k - 1][roles[-1]] if k > 0 else start
+            vals.append(a.elapsed_time(evs[k][r]))
+        return statistics.fmean(vals)
 
-    per = {}
+    # (B) per-phase breakdown: the step-by-step entry points, events around each phase
+    nph = max(3, min(args.steps, 50))
+    for _ in range(2):
+        phased_step({r: [mk() for _ in range(4)] for r in roles})
+    pev = [{r: [mk() for _ in range(4)] for r in roles} for _ in range(nph)]
+    torch.cuda.synchronize()
+    p0 = datetime.datetime.now()
+    for k in range(nph):
+        phased_step(pev[k])
+    torch.cuda.synchronize()
+    p1 = datetime.datetime.now()
+    clocks.mark(p0, p1, "phases")
+    check_device("after timing")
+
+    def mean_ms(r, a, b):
+        return statistics.fmean(e[r][a].elapsed_time(e[r][b]) for e in pev)
+
     pk, pk_kind = peaks()
-    for name in (DECODE, PREFILL):
-        cfg = bufs[name].cfg
-        touched = int((bufs[name].counts.cpu().numpy() > 0).sum())
-        layer_ms = mean_ms(name, 0, 3)
-        ffn_ms = mean_ms(name, 1, 2)
+    per = {}
+    for r in roles:
+        cfg = bufs[r].cfg
+        touched = int((bufs[r].counts.cpu().numpy() > 0).sum())
+        lm = layer_ms(r)
+        fm = mean_ms(r, 1, 2)
         R = cfg.T * cfg.top_k
-        ffn_flops = 6.0 * R * cfg.dim * cfg.hidden
         ffn_bytes = touched * 3 * cfg.dim * cfg.hidden * 2 + 2 * R * cfg.dim * 2
         t_roof = max(alg_flops(cfg) / (pk["bf16_tflops"] * 1e12),
                      alg_bytes(cfg, touched) / (pk["hbm_gbs"] * 1e9))
-        per[name] = {
-            "T": cfg.T, "layer_ms": layer_ms, "tokens_per_s": cfg.T / (layer_ms * 1e-3),
-            "router_permute_ms": mean_ms(name, 0, 1), "ffn_ms": ffn_ms,
-            "combine_ms": mean_ms(name, 2, 3), "experts_touched": touched,
-            "layer_roofline_frac": t_roof / (layer_ms * 1e-3),
-            "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
-            "ffn_hbm_gbs": ffn_bytes / (ffn_ms * 1e-3) / 1e9,
+        per[r] = {
+            "T": cfg.T, "layer_ms": lm, "tokens_per_s": cfg.T / (lm * 1e-3),
+            "layer_roofline_frac": t_roof / (lm * 1e-3),
+            "experts_touched": touched,
+            "phases_ms": {"router_permute": mean_ms(r, 0, 1), "ffn": fm,
+                          "combine": mean_ms(r, 2, 3), "sum": mean_ms(r, 0, 3)},
+            "ffn_tflops": ffn_flops(cfg) / (fm * 1e-3) / 1e12,
+            "ffn_hbm_gbs": ffn_bytes / (fm * 1e-3) / 1e9,
         }
-    pre = per[PREFILL]
-    dec = per[DECODE]
-    dec["roofline"] = {"bound": "hbm", "achieved": dec["ffn_hbm_gbs"], "peak": pk["hbm_gbs"],
-                       "unit": "GB/s", "frac": dec["ffn_hbm_gbs"] / pk["hbm_gbs"],
-                       "kernel": "expert FFN, weight-stream layout (2 tcgen05 kernels)",
-                       "peak_kind": pk_kind}
+        if r == DECODE:
+            per[r]["roofline"] = {"bound": "hbm", "achieved": per[r]["ffn_hbm_gbs"],
+                                  "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                  "frac": per[r]["ffn_hbm_gbs"] / pk["hbm_gbs"],
+                                  "kernel": "expert FFN, weight-stream layout (2 tcgen05 kernels)",
+                                  "peak_kind": pk_kind}
 
-    # end to end (see E2E): copies of every step's x and y are inside the timed region
+    # (C) end to end (see E2E): copies of every step's x and y are inside the timed region
     e2e = E2E(bufs, stream)
     for k in range(args.warmup):
         e2e.step(k)
@@ -669,48 +922,83 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), world) / args.steps
-    for b in bufs.values():
-        st = moe.moe_check_error(b.ws)
-        if st != moe.MOE_OK:
-            raise RuntimeError("device error word after timing: %d" % st)
+    check_device("after the end-to-end loop")
+    clk = clocks.stop("timed")
+    clk_ph = clocks.stop("phases")
 
-    tokens = sum(layers[n][0].T for n in (DECODE, PREFILL))
-    io_bytes = sum(2 * layers[n][0].T * layers[n][0].dim for n in (DECODE, PREFILL))
+    # outputs of the timed build, for the parity check (the layer is deterministic)
+    for r in roles:
+        bufs[r].forward()
+    torch.cuda.synchronize()
+
+    main = per[main_role]
+    main_cfg = bufs[main_role].cfg
+    traffic = recorded_traffic() if args.workload == "mixtral" else None
+    tokens = sum(layers[r][0].T for r in roles)
+    io_bytes = sum(2 * layers[r][0].T * layers[r][0].dim for r in roles)
     result = {
-        "metric": metric, "value": job_tokens_per_s(tokens, world, ms_step), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": wl["metric"], "value": job_tokens_per_s(tokens, world, ms_step),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator, Table 1 shapes, random-init weights)",
         "config": config_block(layers),
-        # the kernel is timed inside a ~1 s back-to-back loop (power cap reached):
-        # its denominator is the sustained measured peak; the burst fraction is kept beside it
-        "roofline": {**ffn_roofline(pre, pk, pk_kind, recorded_traffic()
-                                    if args.workload == "mixtral" else None),
-                     "frac_of_burst_tensor": pre["ffn_tflops"] / pk["bf16_tflops"],
-                     "algorithmic_flop_per_launch": 6.0 * bufs[PREFILL].cfg.T
-                     * bufs[PREFILL].cfg.top_k * bufs[PREFILL].cfg.dim
-                     * bufs[PREFILL].cfg.hidden,
-                     "kernel": "prefill expert FFN: gate/up + down tcgen05 grouped GEMMs "
-                               "(one moe_expert_ffn_grouped call)"},
+        # the expert FFN of the tensor-bound batch, timed in the per-phase loop
+        # (its own clock record decides burst or sustained peak)
+        "roofline": {**ffn_roofline(main, pk, pk_kind, traffic, clk_ph),
+                     "algorithmic_flop_per_launch": ffn_flops(main_cfg),
+                     "launch_ms": main["phases_ms"]["ffn"],
+                     "kernel": "%s expert FFN: gate/up + down tcgen05 grouped GEMMs "
+                               "(one moe_expert_ffn_grouped call)" % main_role,
+                     "clocks": clk_ph},
         "layers": per,
         "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * sum(kernels_per_layer(layers[n][0]) for n in (DECODE, PREFILL)),
+        "gpu_launches": args.steps * sum(kernels_per_layer(layers[r][0]) for r in roles),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host_layers = {n: layers[n] for n in (DECODE, PREFILL)}
-        tok, secs = oracle_sample(host_layers, 32)
+        from oracle import moe_oracle as orc
+        counts = {r: (None if layers[r][0].T <= 16 else (32 if len(roles) > 1 else 64))
+                  for r in roles}
+        tok, secs, refs = oracle_sample(layers, counts)
+        parts = []
+        for r, (rows, ref_y, ref_ids, logits) in refs.items():
+            idx = torch.as_tensor(rows, device="cuda")
+            got_y = orc.widen_bf16(bufs[r].y[idx].view(torch.int16).cpu().numpy().view(np.uint16))
+            got_ids = bufs[r].ids[idx].cpu().numpy()
+            parts.append(parity_check(got_y, got_ids, ref_y, ref_ids, logits,
+                                      layers[r][0].top_k))
         result["cpu_baseline"] = {
             "value": tok / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": "fp64 oracle: decode batch (16 tokens) + 32 seeded prefill tokens, "
-                      "%.1f s" % secs}
+            "sample": "fp64 oracle: %s seeded tokens of the step's batches, %.1f s"
+                      % (" + ".join("%d %s" % (len(refs[r][0]), r) for r in refs), secs)}
+        result["parity"] = merge_parity(parts)
     if rank == 0:
         print(json.dumps(result), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    if result.get("parity") is not None and not result["parity"]["ok"]:
+        raise SystemExit("parity check against the oracle failed")
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        elif args.profile is not None:
+            run_profile_case(args)
+        elif args.workload == "backward":
+            run_backward_bench(args, rank, world)
+        elif args.workload == "stack":
+            run_stack_bench(args, rank, world)
+        else:
+            run_layers_bench(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -41,9 +41,9 @@ Readings where the pages are silent:
   and consecutive pairs whose K chosen experts intersect.
 
 Precision: every input is widened exactly from bf16 to float64 and every step
-runs in float64.  ``h_bf16=True`` additionally rounds the SwiGLU activations to
-bf16 before the down projection (the rounding point of the GPU path); parity
-uses the exact mode.
+runs in float64; nothing is rounded to a narrower type except where the method
+itself defines a bf16 value (the RMSNorm output of the stack workload).  The
+oracle has no mode that imitates the rounding points of any implementation.
 """
 from __future__ import annotations
 
@@ -132,27 +132,24 @@ def expert_weight_shapes(dim: int, hidden: int):
     return [(hidden, dim), (hidden, dim), (dim, hidden)]
 
 
-def expert_hidden(xr, w1, w3, h_bf16: bool = False) -> np.ndarray:
+def expert_hidden(xr, w1, w3) -> np.ndarray:
     """SwiGLU activations SiLU(W1 x) * (W3 x) for the rows of ``xr`` ([m, dim] -> [m, hidden])."""
     xr, w1, w3 = _f64(xr), _f64(w1), _f64(w3)
     assert w1.shape == w3.shape and w1.shape[1] == xr.shape[1]
-    s = silu(xr @ w1.T) * (xr @ w3.T)
-    if h_bf16:
-        s = widen_bf16(round_bf16(s))
-    return s
+    return silu(xr @ w1.T) * (xr @ w3.T)
 
 
-def expert_ffn(xr, w1, w3, w2, h_bf16: bool = False) -> np.ndarray:
+def expert_ffn(xr, w1, w3, w2) -> np.ndarray:
     """E(x) = W2 (SiLU(W1 x) * (W3 x)) applied to each row of ``xr`` ([m, dim] -> [m, dim])."""
     w2 = _f64(w2)
-    s = expert_hidden(xr, w1, w3, h_bf16)
+    s = expert_hidden(xr, w1, w3)
     assert w2.shape == (np.asarray(xr).shape[1], s.shape[1])
     return s @ w2.T
 
 
 # ---------------------------------------------------------- the layer ----
 
-def moe_layer(x, w_gate, w1, w3, w2, top_k: int, h_bf16: bool = False):
+def moe_layer(x, w_gate, w1, w3, w2, top_k: int):
     """Sparse MoE layer forward (§2.1, the top-2 SwiGLU form of the layer).
 
     x: [T, dim]; w_gate: [dim, n]; w1, w3: [n, hidden, dim]; w2: [n, dim, hidden].
@@ -168,7 +165,7 @@ def moe_layer(x, w_gate, w1, w3, w2, top_k: int, h_bf16: bool = False):
         tok, slot = np.nonzero(ids == e)
         if len(tok) == 0:
             continue
-        out = expert_ffn(xf[tok], w1[e], w3[e], w2[e], h_bf16)
+        out = expert_ffn(xf[tok], w1[e], w3[e], w2[e])
         y[tok] += gates[tok, slot][:, None] * out
     return y, ids, gates
 
@@ -179,8 +176,7 @@ def silu_grad(a: np.ndarray) -> np.ndarray:
     return sg * (1.0 + a * (1.0 - sg))
 
 
-def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool = False,
-                       weight_grads: bool = True):
+def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, weight_grads: bool = True):
     """Gradients of the sparse MoE layer (§2.1) for an upstream gradient dy.
 
     The routing (which K experts each token uses) is held fixed: TopK is
@@ -196,15 +192,10 @@ def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool 
     Returns dict(dx [T, dim], dwg [dim, n], dw1, dw3 [n, hidden, dim],
     dw2 [n, dim, hidden]), float64.
 
-    bf16_points: round to bf16 where a bf16 pipeline stores intermediates (h,
-    formed from the unrounded pre-activations; the pre-activations a and b
-    kept for the backward; the expert outputs o, g_k dy, da and db, and each
-    expert's input-gradient rows), everything else in fp64; the exact mode
-    (default) rounds nothing.
+    Every step is float64; nothing is rounded.
     weight_grads=False skips dw1 / dw3 / dw2 (returned as None), for callers
     that only need dx and dwg of a few tokens at full model size.
     """
-    rnd = (lambda v: widen_bf16(round_bf16(v))) if bf16_points else (lambda v: v)
     xf, wg = _f64(x), _f64(w_gate)
     g_up = _f64(dy)
     ids, gates, _ = router(xf, wg, top_k)
@@ -224,22 +215,21 @@ def moe_layer_backward(x, w_gate, w1, w3, w2, top_k: int, dy, bf16_points: bool 
             continue
         W1e, W3e, W2e = _f64(w1[e]), _f64(w3[e]), _f64(w2[e])   # one expert at a time
         xe = xf[tok]
-        a_x = xe @ W1e.T
-        b_x = xe @ W3e.T
-        h = rnd(silu(a_x) * b_x)          # h from the unrounded pre-activations
-        a, b = rnd(a_x), rnd(b_x)         # the stored pre-activations feed the backward
+        a = xe @ W1e.T
+        b = xe @ W3e.T
         s = silu(a)
-        o = rnd(h @ W2e.T)
-        do = rnd(gates[tok, slot][:, None] * g_up[tok])
+        h = s * b
+        o = h @ W2e.T
+        do = gates[tok, slot][:, None] * g_up[tok]
         dgate[tok, slot] = np.sum(g_up[tok] * o, axis=1)
         dh = do @ W2e
-        da = rnd(dh * b * silu_grad(a))
-        db = rnd(dh * s)
+        da = dh * b * silu_grad(a)
+        db = dh * s
         if weight_grads:
             dw2[e] += do.T @ h
             dw1[e] += da.T @ xe
             dw3[e] += db.T @ xe
-        np.add.at(dx, tok, rnd(da @ W1e + db @ W3e))
+        np.add.at(dx, tok, da @ W1e + db @ W3e)
     dl_sel = gates * (dgate - np.sum(gates * dgate, axis=1, keepdims=True))
     dl = np.zeros((T, n))
     np.put_along_axis(dl, ids, dl_sel, axis=1)
@@ -343,7 +333,7 @@ def routing_stats(ids: np.ndarray, n_experts: int):
                 pairs=max(T - 1, 0))
 
 
-def grouped_ffn(x_perm, offsets, w1, w3, w2, h_bf16: bool = False):
+def grouped_ffn(x_perm, offsets, w1, w3, w2):
     """Expert FFN over grouped rows: rows [offsets[e], offsets[e+1]) use expert e.
 
     Returns (y_perm [R, dim], hidden activations [R, hidden]), float64.
@@ -356,7 +346,7 @@ def grouped_ffn(x_perm, offsets, w1, w3, w2, h_bf16: bool = False):
     for e in range(n):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
-            hid[lo:hi] = expert_hidden(xp[lo:hi], w1[e], w3[e], h_bf16)
+            hid[lo:hi] = expert_hidden(xp[lo:hi], w1[e], w3[e])
             y_perm[lo:hi] = hid[lo:hi] @ _f64(w2[e]).T
     return y_perm, hid
 

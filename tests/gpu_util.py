@@ -53,3 +53,46 @@ def assert_bf16_close(gpu_bits, ref, what="", atol=ATOL, rtol=RTOL):
                                 idx.tolist(), [float(g[tuple(i)]) for i in idx],
                                 [float(ref[tuple(i)]) for i in idx]))
     return float(err.max()) if err.size else 0.0
+
+
+# ------------------------------------------------------------- canaries ---
+# Out-of-bounds writes cannot be caught by a sanitizer on the test machines,
+# so outputs are handed to the library as the head of a larger buffer whose
+# tail holds a sentinel; a write past the end of an output changes the tail.
+
+CANARY_ROWS = 3
+_SENTINEL = {torch.bfloat16: -12345.0, torch.float32: -1.2345e30, torch.int32: -0x5A5A5A5B,
+             torch.uint8: 0xA5}
+
+
+class Guarded:
+    """``view`` (shape ``shape``) is the head of ``full``; the trailing
+    CANARY_ROWS rows of ``full`` (``tail`` elements for a 1-D buffer, by
+    default CANARY_ROWS * 64) hold a sentinel that ``check()`` requires
+    unchanged.  ``fill`` (optional) is written over the head."""
+
+    def __init__(self, shape, dtype, fill=None, tail=None):
+        shape = tuple(shape)
+        if tail is None:
+            tail = CANARY_ROWS if len(shape) > 1 else CANARY_ROWS * 64
+        self.rows = shape[0]
+        self.full = torch.full((shape[0] + tail, *shape[1:]), _SENTINEL[dtype], dtype=dtype,
+                               device="cuda")
+        self.view = self.full[:shape[0]]
+        if fill is not None:
+            self.view.fill_(fill)
+        self.tail_ref = self.full[shape[0]:].clone()
+
+    def check(self, what=""):
+        tail = self.full[self.rows:].contiguous().view(torch.uint8)
+        ref = self.tail_ref.contiguous().view(torch.uint8)
+        assert torch.equal(tail, ref), "%s: write past the end of the buffer (canary changed)" % what
+
+
+def guarded_workspace(moe, cfg, backward=False):
+    """A workspace of exactly the size the library asks for, followed by 4 KB
+    of sentinel bytes, initialised; returns (ws, Guarded)."""
+    nbytes = moe.moe_backward_workspace_bytes(cfg) if backward else moe.moe_workspace_bytes(cfg)
+    g = Guarded((nbytes,), torch.uint8, tail=4096)
+    moe.moe_workspace_init(g.view)
+    return g.view, g

@@ -1,6 +1,7 @@
 """Host-side arithmetic of bench.py (no GPU): the algorithmic work the roofline
-divides by, the whole-job throughput, the choice of binding peak, the traffic
-record's source guard, the clock-record parsing and the reference arm's
+divides by, the whole-job throughput, the choice of binding peak (and of the
+burst or sustained tensor peak from the clocks), the traffic record's source
+guard, the clock-record parsing, the parity summary and the reference arm's
 sample sizes."""
 import datetime
 import types
@@ -25,13 +26,44 @@ def test_job_throughput_is_all_ranks_tokens_over_the_slowest_rank():
 
 
 def test_roofline_takes_the_peak_that_binds():
-    pk = {"bf16_tflops_sustained": 1400.0, "hbm_gbs": 6500.0}
-    tensor = bench.ffn_roofline({"ffn_tflops": 1300.0, "ffn_hbm_gbs": 1300.0}, pk, "measured", 7)
-    assert tensor["bound"] == "tensor" and abs(tensor["frac"] - 1300 / 1400) < 1e-12
-    assert tensor["traffic"] == 7
+    pk = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6500.0}
+    at_max = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0}
+    capped = {"sm_mhz": 1400.0, "sm_max_mhz": 2032.0}
+    ffn = {"ffn_tflops": 1300.0, "ffn_hbm_gbs": 1300.0}
+    tensor = bench.ffn_roofline(ffn, pk, "measured", 7, at_max)
+    assert tensor["bound"] == "tensor" and abs(tensor["frac"] - 1300 / 1800) < 1e-12
+    assert tensor["traffic"] == 7 and "burst" in tensor["peak_kind"]
+    sustained = bench.ffn_roofline(ffn, pk, "measured", 7, capped)
+    assert abs(sustained["frac"] - 1300 / 1400) < 1e-12 and "sustained" in sustained["peak_kind"]
+    assert bench.ffn_roofline(ffn, pk, "measured", None)["peak"] == 1800.0   # no record: burst
     hbm = bench.ffn_roofline({"ffn_tflops": 500.0, "ffn_hbm_gbs": 5600.0}, pk, "measured", None)
     assert hbm["bound"] == "hbm" and hbm["unit"] == "GB/s"
     assert abs(hbm["frac"] - 5600 / 6500) < 1e-12
+
+
+def test_tensor_peak_follows_the_clock_record():
+    pk = {"bf16_tflops": 1833.6, "bf16_tflops_sustained": 1423.2}
+    assert bench.tensor_peak(pk, {"sm_mhz": 1940.0, "sm_max_mhz": 2032.0}) == (1833.6, "burst")
+    assert bench.tensor_peak(pk, {"sm_mhz": 1900.0, "sm_max_mhz": 2032.0}) == (1423.2, "sustained")
+    assert bench.tensor_peak(pk, {"sm_mhz": None, "sm_max_mhz": None}) == (1833.6, "burst")
+    assert bench.tensor_peak(pk, None) == (1833.6, "burst")
+
+
+def test_parity_summary_applies_the_north_star_tolerance():
+    import numpy as np
+    ref = np.array([[1.0, -2.0], [0.5, 0.0]])
+    logits = np.array([[3.0, 2.0, 0.0], [3.0, 2.0, 1.995]])     # token 1: 2nd/3rd gap < 1e-2
+    ids = np.array([[0, 1], [0, 1]])
+    ok = bench.parity_check(ref + 0.0095, ids, ref, ids, logits, 2)   # within 1e-2 everywhere
+    assert ok["ok"] and ok["undecided_routing"] == 1 and ok["compared"] == 2
+    bad = bench.parity_check(ref + np.array([[0.0, 0.031], [0, 0]]), ids, ref, ids, logits, 2)
+    assert not bad["ok"] and bad["max_err_over_bound"] > 1.0
+    # another expert on a decided token fails; on an undecided one it is only skipped
+    assert not bench.parity_check(ref, np.array([[0, 2], [0, 1]]), ref, ids, logits, 2)["ok"]
+    skip = bench.parity_check(ref, np.array([[0, 1], [0, 2]]), ref, ids, logits, 2)
+    assert skip["ok"] and skip["compared"] == 1
+    merged = bench.merge_parity([ok, skip])
+    assert merged["tokens"] == 4 and merged["ok"]
 
 
 def test_traffic_record_is_dropped_when_the_kernel_sources_change(monkeypatch):
@@ -44,7 +76,8 @@ def _sampler(lines, t0, t1):
     cs = object.__new__(bench.ClockSampler)
     cs.proc = types.SimpleNamespace(terminate=lambda: None,
                                     communicate=lambda timeout=None: ("\n".join(lines), ""))
-    cs.window = (t0, t1)
+    cs.windows = {"timed": (t0, t1)}
+    cs.rows = None
     return cs
 
 

@@ -2,7 +2,8 @@
 import numpy as np
 
 import moe_inputs as mi
-from tests.inputs_filtered import ambiguous_tokens, filtered_layer
+from tests.inputs_filtered import (TOKEN_TILE, align_slots, ambiguous_tokens, filtered_layer,
+                                   tile_sample)
 
 
 def test_c_and_numpy_streams_agree():
@@ -65,3 +66,33 @@ def test_skewed_tokens_follow_zipf_top1():
     share = np.bincount(ids[:, 0], minlength=8) / cfg.T
     assert np.max(np.abs(share - mi.zipf_shares(8, 1.2))) < 0.03
     assert 0.38 < share[0] < 0.48
+
+
+def test_tile_sample_covers_every_tile():
+    # the full-size parity sampler on a hand-built grouping: experts of 0, 1,
+    # 256, 257 and 600 rows; every tile must contribute its first and last row
+    counts = np.array([0, 1, 256, 257, 600])
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    perm_src = np.arange(offsets[-1])          # identity: token == grouped row
+    toks = set(tile_sample(offsets, perm_src).tolist())
+    n_tiles = 0
+    for e in range(len(counts)):
+        for t0 in range(offsets[e], offsets[e + 1], TOKEN_TILE):
+            t1 = min(t0 + TOKEN_TILE, offsets[e + 1])
+            assert t0 in toks and t1 - 1 in toks
+            n_tiles += 1
+    assert n_tiles == 0 + 1 + 1 + 2 + 3
+    assert offsets[-1] - 1 in toks             # the last row of the last partial tile
+    assert 1 + 256 + 128 in toks               # both sides of the middle of a full tile
+
+
+def test_align_slots_accepts_only_reordered_undecided_tokens():
+    import pytest
+    ref = np.array([[0, 1], [2, 3], [4, 5]])
+    got = np.array([[0, 1], [3, 2], [4, 5]])
+    p = align_slots(got, ref, np.array([True, False, True]))
+    assert p.tolist() == [[0, 1], [1, 0], [0, 1]]
+    with pytest.raises(AssertionError):        # order decided: a swap is an error
+        align_slots(got, ref, np.array([True, True, True]))
+    with pytest.raises(AssertionError):        # another expert is always an error
+        align_slots(np.array([[0, 1], [2, 6], [4, 5]]), ref, np.array([False] * 3))

@@ -406,18 +406,36 @@ def test_backward_single_expert_is_the_dense_swiglu_gradient():
     assert np.max(np.abs(dw2 - g["dw2"][0])) < 1e-12
 
 
-def test_backward_bf16_points_mode_stays_near_exact():
-    """The rounding-matched backward differs from the exact one by bf16-sized
-    errors only (and equals it when nothing needs rounding)."""
+def test_gpu_rounding_model_stays_near_exact():
+    """The model of the CUDA backward's bf16 storage points (test code, not the
+    oracle) differs from the exact oracle by bf16-sized amounts only."""
+    from tests.gpu_rounding_model import backward_at_gpu_storage_points
     rng = np.random.default_rng(71)
     x, wg, w1, w3, w2 = _rand_layer(rng, 40, 16, 24, 8)
     dy = orc.widen_bf16(orc.round_bf16(rng.standard_normal((40, 16))))
     a = orc.moe_layer_backward(x, wg, w1, w3, w2, 2, dy)
-    b = orc.moe_layer_backward(x, wg, w1, w3, w2, 2, dy, bf16_points=True)
+    b = backward_at_gpu_storage_points(x, wg, w1, w3, w2, 2, dy)
     for k in a:
         rms = np.sqrt(np.mean(a[k] ** 2))
         assert np.max(np.abs(a[k] - b[k])) < 0.1 * rms, k
         assert np.max(np.abs(a[k] - b[k])) > 0, k
+
+
+def test_gpu_rounding_model_is_exact_where_nothing_rounds():
+    """With every intermediate exactly representable in bf16 (small integers
+    and zero router weight), the storage-point model equals the exact oracle."""
+    from tests.gpu_rounding_model import backward_at_gpu_storage_points
+    T, d, h = 3, 2, 2
+    x = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    wg = np.zeros((d, 1))
+    w1 = np.full((1, h, d), 0.0)          # a = 0: SiLU(0) = 0, SiLU'(0) = 1/2
+    w3 = np.array([[[1.0, 0.0], [0.0, 2.0]]])
+    w2 = np.array([[[1.0, 1.0], [0.0, 1.0]]])
+    dy = np.array([[1.0, 2.0], [0.5, 0.0], [1.0, 1.0]])
+    a = orc.moe_layer_backward(x, wg, w1, w3, w2, 1, dy)
+    b = backward_at_gpu_storage_points(x, wg, w1, w3, w2, 1, dy)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
 
 
 def test_backward_unit_gradients_match_the_full_backward():

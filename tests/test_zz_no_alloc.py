@@ -29,32 +29,50 @@ def _host(outs):
 def _case(T, n, K, dim, seed):
     cfg = mi.Config("noalloc", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=seed)
     rng = np.random.default_rng(seed)
-    ids = np.stack([rng.permutation(n)[:K] for _ in range(T)]).astype(np.int32)
+    ids = np.argsort(rng.random((T, n)), axis=1)[:, :K].astype(np.int32)
     return cfg, dev_bf16(mi.gen_x(cfg)), dev_i32(ids)
 
 
-def test_noalloc_grouping_equals_workspace_grouping_twice():
+def _check_same(cfg, x, ids):
     moe = lib()
-    # two calls in a row with different shapes: the shared scratch keeps the
-    # first call's contents, which the second call must not depend on
-    for T, n, K, dim, seed in [(3000, 8, 2, 256, 11), (129, 5, 3, 128, 12)]:
-        cfg, x, ids = _case(T, n, K, dim, seed)
-        ref = _outputs(cfg)
-        moe.moe_permute(cfg, x, ids, *ref, moe.new_workspace(cfg))
-        got = _outputs(cfg)
-        moe.moe_permute_noalloc(cfg, x, ids, *got)
-        torch.cuda.synchronize()
-        for a, b in zip(_host(got), _host(ref)):
-            assert np.array_equal(a, b)
+    ref = _outputs(cfg)
+    moe.moe_permute(cfg, x, ids, *ref, moe.new_workspace(cfg))
+    got = _outputs(cfg)
+    moe.moe_permute_noalloc(cfg, x, ids, *got)
+    torch.cuda.synchronize()
+    for a, b in zip(_host(got), _host(ref)):
+        assert np.array_equal(a, b)
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # the library itself refuses a batch beyond its fixed scratch before it
-    # enqueues anything; called through the C entry point, because the Python
-    # binding already refuses these tensors as too small for the shape
+def test_noalloc_grouping_equals_workspace_grouping_twice():
+    # two calls in a row, both above the 2048 assignments that a single block
+    # groups on its own, so both go through the shared scratch tables: the
+    # first with the larger table (24 chunks x 16 experts), the second with a
+    # smaller one (12 chunks x 8 experts) that must not depend on what the
+    # first call left in the scratch
+    for T, n, K, dim, seed in [(3000, 16, 2, 256, 11), (1500, 8, 2, 128, 12)]:
+        R = T * K
+        assert R > 2048
+        _check_same(*_case(T, n, K, dim, seed))
+
+
+def test_noalloc_grouping_at_the_scratch_limit():
+    # ceil(T*K / 256) * n == 65536 exactly (256 chunks x 256 experts): the
+    # largest table the fixed scratch holds is accepted and matches moe_permute
+    cfg, x, ids = _case(8192, 256, 8, 128, 13)
+    assert -(-cfg.T * cfg.top_k // 256) * cfg.n_experts == 65536
+    _check_same(cfg, x, ids)
+
+
+@pytest.mark.parametrize("T,n,K", [(2_200_000, 8, 1), (65_537, 256, 1)])
+def test_noalloc_rejects_shapes_beyond_its_scratch(T, n, K):
+    # the library itself refuses a batch beyond its fixed scratch (here one
+    # chunk past it: 257 chunks x 256 experts) before it enqueues anything;
+    # called through the C entry point, because the Python binding already
+    # refuses these tensors as too small for the shape
     import ctypes
     moe = lib()
-    s = moe.make_shape(T=2_200_000, dim=128, hidden=128, n_experts=8, top_k=1)
+    s = moe.make_shape(T=T, dim=128, hidden=128, n_experts=n, top_k=K)
     small = _outputs(mi.Config("s", T=1, dim=128, hidden=128, top_k=1))
     x = torch.zeros((1, 128), dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
