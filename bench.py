@@ -3,18 +3,19 @@
 A step is one pass of the whole hot path over two batches of synthetic
 Mixtral-shaped tokens (dim 4096, hidden 14336, 8 experts, top-2; Table 1 of
 "Mixtral of Experts"): a decode-sized layer call (T=16, weight-bandwidth
-bound, small-T weight-stream FFN) and a prefill-sized layer call (T=4096,
-tensor-core bound, CTA-pair grouped-GEMM FFN), each one moe_layer_forward call
-(router -> grouping -> expert FFN -> combine) through the C ABI on resident
+bound: one moe_layer_forward call, which routes, groups and gathers the batch
+in one launch and streams the expert weights in one more) and a prefill-sized
+layer (T=4096, tensor-core bound: router -> grouping -> expert FFN -> combine
+through the step-by-step entry points, with CUDA events on both sides of the
+expert FFN -- the roofline unit, its two tcgen05 CTA-pair grouped GEMMs -- so
+that it is timed inside the timed region), all through the C ABI on resident
 inputs.  value = tokens of both batches per second of step time.
 
-Beside it: per-layer times; a per-phase breakdown (router + grouping, expert
-FFN, combine) from a second loop of the step-by-step entry points, which also
-times the dominant unit for the roofline (the prefill expert FFN: its two
-tcgen05 grouped-GEMM kernels); the end-to-end rate with host copies; the
-fp64 oracle timed on the host cores; and a parity check of the timed build's
-outputs against that oracle on the tokens it evaluated (the run fails if
-they disagree).
+Beside it: per-layer times; a per-phase breakdown of both batches from a
+second loop of the step-by-step entry points; the end-to-end rate with host
+copies (moe_layer_forward for both batches); the fp64 oracle timed on the
+host cores; and a parity check of the timed build's outputs against that
+oracle on the tokens it evaluated (the run fails if they disagree).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mixtral|fine|skew|stack|backward]
@@ -251,11 +252,16 @@ class E2E:
                     self.compute.wait_event(s["down"])
 
 
-# Kernels of ours launched per layer call (moe_layer_forward): router, grouping
-# (one kernel up to 2048 assignments, histogram / scan / scatter above), gather,
-# gate/up GEMM, down GEMM, combine.
+# Kernels of ours launched per layer call (moe_layer_forward): routing (one
+# launch for a decode-sized batch of T <= 32 tokens over n <= 8 experts; else
+# router, grouping -- one kernel up to 2048 assignments, histogram / scan /
+# scatter above -- and gather), gate/up GEMM, down GEMM, combine.
 def kernels_per_layer(cfg):
-    return 1 + (3 if cfg.T * cfg.top_k > 2048 else 1) + 1 + 2 + 1
+    if cfg.T <= 32 and cfg.n_experts <= 8 and cfg.rmsnorm_eps == 0:
+        routing = 1
+    else:
+        routing = 1 + (3 if cfg.T * cfg.top_k > 2048 else 1) + 1
+    return routing + 2 + 1
 
 
 # --------------------------------------------------------------- clocks ---
@@ -805,9 +811,23 @@ def run_layers_bench(args, rank, world):
     stream = torch.cuda.current_stream()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def fused_step(ev=None):
+    def timed_step(ev=None):
+        """One step: every batch but the main one through moe_layer_forward; the
+        main batch through the step-by-step entry points with an event on each
+        side of its expert FFN, so that the roofline unit is timed in the same
+        region, under the same clocks, as the step."""
         for r in roles:
-            bufs[r].forward()
+            b = bufs[r]
+            if r == main_role:
+                b.router_permute()
+                if ev is not None:
+                    ev["ffn0"].record(stream)
+                b.ffn()
+                if ev is not None:
+                    ev["ffn1"].record(stream)
+                b.combine()
+            else:
+                b.forward()
             if ev is not None:
                 ev[r].record(stream)
 
@@ -829,20 +849,21 @@ def run_layers_bench(args, rank, world):
                 raise RuntimeError("device error word %s: %d" % (when, st))
 
     for _ in range(args.warmup):
-        fused_step()
+        timed_step()
     torch.cuda.synchronize()
     check_device("after warm-up")
 
-    # (A) the timed region: the step through moe_layer_forward, one event per layer
+    # (A) the timed region: K steps, an event after each layer and on both
+    # sides of the main batch's expert FFN
     clocks = ClockSampler()
-    evs = [{r: mk() for r in roles} for _ in range(args.steps)]
+    evs = [dict({r: mk() for r in roles}, ffn0=mk(), ffn1=mk()) for _ in range(args.steps)]
     start = mk()
     barrier(world)
     torch.cuda.synchronize()
     w0 = datetime.datetime.now()
     start.record(stream)
     for k in range(args.steps):
-        fused_step(evs[k])
+        timed_step(evs[k])
     torch.cuda.synchronize()
     w1 = datetime.datetime.now()
     barrier(world)
@@ -861,7 +882,10 @@ def run_layers_bench(args, rank, world):
             vals.append(a.elapsed_time(evs[k][r]))
         return statistics.fmean(vals)
 
-    # (B) per-phase breakdown: the step-by-step entry points, events around each phase
+    main_ffn_ms = statistics.fmean(e["ffn0"].elapsed_time(e["ffn1"]) for e in evs)
+
+    # (B) per-phase breakdown of every batch: the step-by-step entry points,
+    # events around each phase (informational; the roofline unit is timed in A)
     nph = max(3, min(args.steps, 50))
     for _ in range(2):
         phased_step({r: [mk() for _ in range(4)] for r in roles})
@@ -884,7 +908,7 @@ def run_layers_bench(args, rank, world):
         cfg = bufs[r].cfg
         touched = int((bufs[r].counts.cpu().numpy() > 0).sum())
         lm = layer_ms(r)
-        fm = mean_ms(r, 1, 2)
+        fm = main_ffn_ms if r == main_role else mean_ms(r, 1, 2)
         R = cfg.T * cfg.top_k
         ffn_bytes = touched * 3 * cfg.dim * cfg.hidden * 2 + 2 * R * cfg.dim * 2
         t_roof = max(alg_flops(cfg) / (pk["bf16_tflops"] * 1e12),
@@ -892,8 +916,11 @@ def run_layers_bench(args, rank, world):
         per[r] = {
             "T": cfg.T, "layer_ms": lm, "tokens_per_s": cfg.T / (lm * 1e-3),
             "layer_roofline_frac": t_roof / (lm * 1e-3),
+            "layer_call": "step-by-step entry points" if r == main_role else "moe_layer_forward",
             "experts_touched": touched,
-            "phases_ms": {"router_permute": mean_ms(r, 0, 1), "ffn": fm,
+            "ffn_ms": fm,
+            "ffn_timed_in": "timed region" if r == main_role else "phase loop",
+            "phases_ms": {"router_permute": mean_ms(r, 0, 1), "ffn": mean_ms(r, 1, 2),
                           "combine": mean_ms(r, 2, 3), "sum": mean_ms(r, 0, 3)},
             "ffn_tflops": ffn_flops(cfg) / (fm * 1e-3) / 1e12,
             "ffn_hbm_gbs": ffn_bytes / (fm * 1e-3) / 1e9,
@@ -902,7 +929,8 @@ def run_layers_bench(args, rank, world):
             per[r]["roofline"] = {"bound": "hbm", "achieved": per[r]["ffn_hbm_gbs"],
                                   "peak": pk["hbm_gbs"], "unit": "GB/s",
                                   "frac": per[r]["ffn_hbm_gbs"] / pk["hbm_gbs"],
-                                  "kernel": "expert FFN, weight-stream layout (2 tcgen05 kernels)",
+                                  "kernel": "expert FFN, weight-stream layout (one tcgen05 "
+                                            "kernel, both passes)",
                                   "peak_kind": pk_kind}
 
     # (C) end to end (see E2E): copies of every step's x and y are inside the timed region
@@ -923,13 +951,13 @@ def run_layers_bench(args, rank, world):
     barrier(world)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), world) / args.steps
     check_device("after the end-to-end loop")
-    clk = clocks.stop("timed")
-    clk_ph = clocks.stop("phases")
 
     # outputs of the timed build, for the parity check (the layer is deterministic)
     for r in roles:
         bufs[r].forward()
     torch.cuda.synchronize()
+    clk = clocks.stop("timed")
+    clk_ph = clocks.stop("phases")
 
     main = per[main_role]
     main_cfg = bufs[main_role].cfg
@@ -943,14 +971,14 @@ def run_layers_bench(args, rank, world):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator, Table 1 shapes, random-init weights)",
         "config": config_block(layers),
-        # the expert FFN of the tensor-bound batch, timed in the per-phase loop
-        # (its own clock record decides burst or sustained peak)
-        "roofline": {**ffn_roofline(main, pk, pk_kind, traffic, clk_ph),
+        # the expert FFN of the tensor-bound batch, timed with events inside the
+        # timed region (its clock record decides burst or sustained peak)
+        "roofline": {**ffn_roofline(main, pk, pk_kind, traffic, clk),
                      "algorithmic_flop_per_launch": ffn_flops(main_cfg),
-                     "launch_ms": main["phases_ms"]["ffn"],
+                     "launch_ms": main["ffn_ms"],
                      "kernel": "%s expert FFN: gate/up + down tcgen05 grouped GEMMs "
-                               "(one moe_expert_ffn_grouped call)" % main_role,
-                     "clocks": clk_ph},
+                               "(one moe_expert_ffn_grouped call)" % main_role},
+        "phase_loop_clocks": clk_ph,
         "layers": per,
         "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,

@@ -44,6 +44,7 @@ WsLayout ws_layout(const moe_shape* s) {
   L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
   size_t off = 0;
   L.err = off;
+  L.grid_bar = kWsGridBarOffset;
   L.counters = kWsHeaderBytes;
   off += kWsControlBytes;  // control region: error word, stream-K counters
   auto take = [&](size_t bytes) {
@@ -214,7 +215,7 @@ moe_status moe_expert_ffn_grouped(const moe_shape* shape, const moe_bf16* x_perm
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const cudaError_t e = launch_expert_ffn(*shape, x_perm, offsets, w1, w3, w2, h, y_perm, path,
                                           at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
-                                          at<int>(ws, L.counters),
+                                          at<int>(ws, L.counters), at<unsigned>(ws, L.grid_bar),
                                           static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
@@ -260,18 +261,27 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   uint16_t* u = norm ? at<uint16_t>(ws, L.u) : nullptr;
   const uint16_t* src = norm ? u : x;
 
-  // the grouping recounts the assignments from the ids: the router writes no counts
-  cudaError_t e = launch_router(*shape, x, w_gate, d_ids, d_gates, nullptr, u,
-                                norm ? opts->rmsnorm_eps : 0.0f, at<uint32_t>(ws, L.err), st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_permute(*shape, src, d_ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
-                     at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src),
-                     at<int32_t>(ws, L.slot_row), at<uint16_t>(ws, L.x_perm), L.nchunks, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e;
+  if (!norm && route_small_supported(*shape)) {
+    // decode-sized batch: routing, grouping and gather in one launch
+    e = launch_route_small(*shape, x, w_gate, d_ids, d_gates, offsets,
+                           at<int32_t>(ws, L.perm_src), at<int32_t>(ws, L.slot_row),
+                           at<uint16_t>(ws, L.x_perm), st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    // the grouping recounts the assignments from the ids: the router writes no counts
+    e = launch_router(*shape, x, w_gate, d_ids, d_gates, nullptr, u,
+                      norm ? opts->rmsnorm_eps : 0.0f, at<uint32_t>(ws, L.err), st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_permute(*shape, src, d_ids, nullptr, offsets, at<int32_t>(ws, L.chunk_hist),
+                       at<int32_t>(ws, L.chunk_base), at<int32_t>(ws, L.perm_src),
+                       at<int32_t>(ws, L.slot_row), at<uint16_t>(ws, L.x_perm), L.nchunks, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   e = launch_expert_ffn(*shape, at<uint16_t>(ws, L.x_perm), offsets, w1, w3, w2,
                         at<uint16_t>(ws, L.h), at<uint16_t>(ws, L.y_perm), path,
                         at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
-                        at<int>(ws, L.counters), st);
+                        at<int>(ws, L.counters), at<unsigned>(ws, L.grid_bar), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_combine(*shape, at<uint16_t>(ws, L.y_perm), at<int32_t>(ws, L.slot_row), d_gates,
                      residual, y, st);

@@ -1,8 +1,10 @@
 """Whole MoE layer on the GPU against the fp64 oracle, on the Mixtral-shaped
 workloads: routing (ids, counts, offsets, permutation) bit-exact on every
 token, outputs within |gpu - oracle| <= 1e-2 + 1e-2 |oracle| on every token
-the oracle evaluates, and the fused entry point bit-identical to the
-step-by-step calls.
+the oracle evaluates, for the step-by-step calls and for the fused entry
+point.  Where both route with the same kernels (every batch but the
+decode-sized one, which moe_layer_forward routes, groups and gathers in one
+launch) the two are also bit-identical.
 
 Which tokens the oracle evaluates: all of them in the small cases.  At full
 size, a stratified sample (``tile_sample``) that puts checked rows in EVERY
@@ -81,14 +83,21 @@ def fused(cfg, dev, path):
     moe = lib()
     y = Guarded((cfg.T, cfg.dim), torch.bfloat16, float("nan"))
     ids = Guarded((cfg.T, cfg.top_k), torch.int32, -7)
+    gates = Guarded((cfg.T, cfg.top_k), torch.float32, -7.0)
     ws, wsg = guarded_workspace(moe, cfg)
     moe.moe_layer_forward(cfg, dev["x"], dev["wg"], dev["w1"], dev["w3"], dev["w2"], y.view, ws,
-                          ids=ids.view, ffn_path=path)
+                          ids=ids.view, gates=gates.view, ffn_path=path)
     assert moe.moe_check_error(ws) == moe.MOE_OK
     y.check("y (fused)")
     ids.check("ids (fused)")
+    gates.check("gates (fused)")
     wsg.check("workspace (fused)")
-    return host_bits(y.view), ids.view.cpu().numpy()
+    return host_bits(y.view), ids.view.cpu().numpy(), gates.view.cpu().numpy()
+
+
+def fused_routes_in_one_launch(cfg):
+    """moe_layer_forward's decode-sized routing kernel: T <= 32, n <= 8."""
+    return cfg.T <= 32 and cfg.n_experts <= 8
 
 
 def check_layer(name, path, sample=None):
@@ -99,8 +108,8 @@ def check_layer(name, path, sample=None):
     got = stepwise(cfg, dev, path)
     # routing: every token, bit-exact (slot order compared where it is decided)
     r_ids, r_gates, _ = orc.router(L.x, L.wg, cfg.top_k)
-    p = check_routing(got["ids"], got["gates"], r_ids, r_gates,
-                      order_decided(L.x, L.wg, cfg.top_k))
+    decided = order_decided(L.x, L.wg, cfg.top_k)
+    p = check_routing(got["ids"], got["gates"], r_ids, r_gates, decided)
     counts, offsets, perm_src, slot_row = orc.routing_tables(r_ids, cfg.n_experts)
     assert np.array_equal(got["counts"], counts)
     assert np.array_equal(got["offsets"], offsets)
@@ -114,10 +123,15 @@ def check_layer(name, path, sample=None):
         rows = np.union1d(tile_sample(offsets, perm_src), rnd)
     ref, _, _ = orc.moe_layer(L.x[rows], L.wg, L.w1, L.w3, L.w2, cfg.top_k)
     assert_bf16_close(got["y"][rows], ref, "%s layer output" % name)
-    # the fused entry point runs the same kernels: identical bits
-    y_fused, ids_fused = fused(cfg, dev, path)
-    assert np.array_equal(ids_fused, got["ids"])
-    assert np.array_equal(y_fused, got["y"])
+    # the fused entry point
+    y_fused, ids_fused, gates_fused = fused(cfg, dev, path)
+    check_routing(ids_fused, gates_fused, r_ids, r_gates, decided)
+    if fused_routes_in_one_launch(cfg):
+        assert_bf16_close(y_fused[rows], ref, "%s fused layer output" % name)
+    else:
+        # the same kernels: identical bits
+        assert np.array_equal(ids_fused, got["ids"])
+        assert np.array_equal(y_fused, got["y"])
     return rows
 
 
@@ -161,6 +175,19 @@ def test_mixtral_8x22b_dims(path):
     # "Mixtral 8x22B, scaling the exact same architecture up": dim 6144, hidden 16384
     cfg = mi.Config("8x22b", T=48, dim=6144, hidden=16384, seed=46108)
     check_layer(cfg, path)
+
+
+@pytest.mark.parametrize("T,dim,n,K", [
+    (1, 128, 8, 2), (32, 128, 8, 2), (17, 256, 8, 8), (9, 384, 5, 3), (32, 512, 1, 1),
+    (20, 128, 8, 1), (31, 4096, 8, 2), (12, 6144, 6, 2)])
+def test_decode_sized_layer_routed_in_one_launch(T, dim, n, K):
+    # moe_layer_forward routes, groups and gathers a batch of T <= 32 tokens
+    # over n <= 8 experts in one launch: edge batches (1 token, 32 tokens),
+    # K = 1, K = n, fewer than 8 experts, 8x22B's model dimension
+    cfg = mi.Config("small-route", T=T, dim=dim, hidden=256, n_experts=n, top_k=K,
+                    seed=46600 + T * 7 + dim + n)
+    assert fused_routes_in_one_launch(cfg)
+    check_layer(cfg, 0)
 
 
 def test_largest_batch_mixtral_dims_sampled():
