@@ -929,8 +929,7 @@ def run_layers_bench(args, rank, world):
             per[r]["roofline"] = {"bound": "hbm", "achieved": per[r]["ffn_hbm_gbs"],
                                   "peak": pk["hbm_gbs"], "unit": "GB/s",
                                   "frac": per[r]["ffn_hbm_gbs"] / pk["hbm_gbs"],
-                                  "kernel": "expert FFN, weight-stream layout (one tcgen05 "
-                                            "kernel, both passes)",
+                                  "kernel": "expert FFN, weight-stream layout (2 tcgen05 kernels)",
                                   "peak_kind": pk_kind}
 
     # (C) end to end (see E2E): copies of every step's x and y are inside the timed region

@@ -13,8 +13,14 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every array argument is caller-owned DEVICE memory, row-major, and must be
- *   16-byte aligned.  The library allocates nothing, keeps no state between
- *   calls and never synchronises the stream, except moe_check_error.
+ *   16-byte aligned.  The library allocates nothing and never synchronises the
+ *   stream, except moe_check_error.  It keeps state between calls in two
+ *   places only, both process-wide device objects: (1) the error word of
+ *   moe_router_topk, which has no workspace -- an expired bounded wait of any
+ *   moe_router_topk call, on any stream, is recorded there, and ANY
+ *   moe_check_error call reports and clears it, whatever workspace it is
+ *   given; (2) the fixed scratch of moe_permute_noalloc (see there).  Every
+ *   other entry point keeps its state in the caller's workspace.
  * - bf16 arrays are raw bfloat16 bit patterns (moe_bf16).
  * - Shapes: x, y [T, dim]; w_gate [dim, n]; w1, w3 [n, hidden, dim];
  *   w2 [n, dim, hidden]; ids [T, K] int32; gates [T, K] float32;
@@ -121,7 +127,10 @@ MOE_API moe_status moe_router_topk(const moe_shape* shape, const moe_bf16* x,
  *   out offsets [n + 1] (exclusive prefix sum of the per-expert counts),
  *   perm_src [T*K] (grouped row -> token), slot_row [T*K] (assignment t*K+k ->
  *   grouped row), x_perm [T*K, dim] (x_perm[r] = x[perm_src[r]], bit copy).
- *   ws: workspace of moe_workspace_bytes(shape) bytes (scratch). */
+ *   ws: workspace of moe_workspace_bytes(shape) bytes (scratch).
+ * The per-expert counts are recounted from ids rather than taken as an input:
+ * a stable order needs the counts of every block of 256 assignments, which
+ * the grouping computes anyway, and their sums are the per-expert counts. */
 MOE_API moe_status moe_permute(const moe_shape* shape, const moe_bf16* x,
                        const int32_t* ids, int32_t* offsets, int32_t* perm_src,
                        int32_t* slot_row, moe_bf16* x_perm, void* ws,
@@ -149,7 +158,11 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const moe_bf16* y_perm,
                        const moe_bf16* residual, moe_bf16* y, void* stream);
 
 /* The whole layer: router -> grouping -> expert FFN -> combine, all on
- * `stream`, no host synchronisation.  ids and gates are optional outputs
+ * `stream`, no host synchronisation.  A decode-sized batch (T <= 32 tokens,
+ * n <= 8 experts, no RMSNorm) is routed, grouped and gathered by one kernel
+ * launch; its logits are summed in another order than moe_router_topk's, so
+ * gates may differ from that entry point's in the last bits (ids agree
+ * wherever the selection is decided).  ids and gates are optional outputs
  * (nullable; kept in the workspace otherwise).  With opts->use_rmsnorm the
  * layer routes and evaluates RMSNorm(x) (bf16, unit gain) and the combine
  * adds opts->residual (pass x for the residual block x + MoE(RMSNorm(x))). */
@@ -195,9 +208,12 @@ MOE_API moe_status moe_layer_backward(const moe_shape* shape, const moe_bf16* x,
 MOE_API moe_status moe_routing_stats(const moe_shape* shape, const int32_t* ids,
                                      int32_t* slot_counts, int32_t* repeats, void* stream);
 
-/* Synchronise `stream`, read and clear the workspace error word.  Returns
- * MOE_ERR_TIMEOUT if any bounded device wait expired since the last check,
- * MOE_ERR_CUDA on a pending CUDA error, MOE_OK otherwise. */
+/* Synchronise `stream`, read and clear the workspace error word and the
+ * process-wide error word of moe_router_topk (see the conventions above).
+ * Returns MOE_ERR_TIMEOUT if any bounded device wait of a call using this
+ * workspace, or of any moe_router_topk call, expired since the last check;
+ * MOE_ERR_CUDA on a pending CUDA error; MOE_OK otherwise.  After
+ * MOE_ERR_TIMEOUT, call moe_workspace_init on the workspace again. */
 MOE_API moe_status moe_check_error(void* ws, void* stream);
 
 /* Diagnostic of the bounded-wait machinery (no counterpart on the pages):

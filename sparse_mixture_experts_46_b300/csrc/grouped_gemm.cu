@@ -338,102 +338,56 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Weight stream, stream-K schedule (small T), both passes in one persistent
-// kernel.  The weight tiles of a pass (expert x 128 weight rows, over the
-// whole reduction) do not divide evenly into the SMs (e.g. 896 gate/up tiles
-// on 148 SMs is 6.05 tiles each), and the pass is HBM-bound, so a whole-tile
-// round robin leaves most SMs idle in the last round.  Here each pass is a
-// list of units (tile, 64-wide K block) and CTA c streams the contiguous units
-// [c*U/G, (c+1)*U/G): every SM moves the same number of weight bytes.  A tile
-// that a CTA covers completely gets the usual epilogue.  A tile split between
-// CTAs: every contributor writes its fp32 accumulator slice to its partial
-// slot in the workspace, publishes it (fence, then an atomic increment of the
-// tile's counter), and the contributor that arrives last sums all slices in
-// CTA order (a fixed order: deterministic), applies the epilogue and resets
-// the counter to zero.  No CTA waits for another inside a pass.
-//
-// Pass 1 (gate/up, H) and pass 2 (down, y_perm) run in the same CTAs, one
-// after the other.  Between them every CTA's epilogue publishes that its pass-1
-// outputs are written (fence, then an increment of a grid counter in the
-// workspace), and the producer of each CTA -- which has meanwhile filled its
-// ring with the first W2 tiles of its pass-2 range, since the weights do not
-// depend on H -- waits (bounded) until all CTAs have published before it loads
-// any H tile.  The pass boundary therefore costs neither a launch nor an empty
-// pipeline.  The grid is one CTA per SM, all resident at once.
-struct StreamPass {
-  uint16_t* out;           // H [R, hidden] (pass 1) or y_perm [R, dim] (pass 2)
+// Weight stream, stream-K schedule (small T).  The weight tiles of one pass
+// (expert x 128 weight rows, over the whole reduction) do not divide evenly
+// into the SMs (e.g. 896 gate/up tiles on 148 SMs is 6.05 tiles each), and
+// the pass is HBM-bound, so a whole-tile round robin leaves most SMs idle in
+// the last round.  Here the pass is a list of units (tile, 64-wide K block)
+// and CTA c streams the contiguous units [c*U/G, (c+1)*U/G): every SM moves
+// the same number of weight bytes.  A tile that a CTA covers completely gets
+// the usual epilogue.  A tile split between CTAs: every contributor writes its
+// fp32 accumulator slice to its partial slot in the workspace, publishes it
+// (fence, then an atomic increment of the tile's counter), and the contributor
+// that arrives last sums all slices in CTA order (a fixed order:
+// deterministic), applies the epilogue and resets the counter to zero.  No CTA
+// waits for another.
+struct StreamKArgs {
+  const int32_t* offsets;  // [n + 1] grouped-row offsets (device)
+  uint16_t* out;           // H [R, hidden] (gate/up) or y_perm [R, dim] (down)
+  uint32_t* err;           // workspace error word
+  uint64_t limit_ns;       // bounded-wait limit
+  int n_experts;
   int k_blocks;            // reduction length / 64
   int w_tiles;             // weight tiles (128 rows) per expert
   int w_rows_per_expert;   // rows of one expert's weight matrix
   int out_ld;              // output row stride in elements
-};
-
-struct StreamKArgs {
-  const int32_t* offsets;  // [n + 1] grouped-row offsets (device)
-  uint32_t* err;           // workspace error word
-  uint64_t limit_ns;       // bounded-wait limit
-  int n_experts;
   int rows_total;          // R
-  float* partials;         // [gridDim][2][128][64] fp32 accumulator slices
+  float* partials;         // [gridDim][2][128][ACC_COLS] fp32 accumulator slices
   int* counters;           // [tiles] arrivals per split tile; zero on entry and exit
-  unsigned* grid_bar;      // [2]: pass-1 completions, producers past the wait; zero on entry/exit
-  StreamPass pass[2];
 };
 
-constexpr int kSkStages1 = 6;    // pass-1 ring: W1 + W3 tiles + 32 token rows (36 KB)
-constexpr int kSkStages2 = 10;   // pass-2 ring: W2 tile + 32 rows of H (20 KB)
-constexpr int kSkPartStride = 64;
-
-struct StreamKCfg {
-  static constexpr int BN = kStreamTokens;
-  static constexpr int TILE = 128 * 128;                  // 128 weight rows x 64 bf16
-  static constexpr int ACT = BN * 128;                    // 32 token rows x 64 bf16
-  static constexpr int STAGE1 = 2 * TILE + ACT;
-  static constexpr int STAGE2 = TILE + ACT;
-  static constexpr int RING = (kSkStages1 * STAGE1 > kSkStages2 * STAGE2) ? kSkStages1 * STAGE1
-                                                                          : kSkStages2 * STAGE2;
-  static constexpr int ACC = 2 * BN;                      // TMEM columns per buffer (pass 1: a | g)
-  static constexpr int TMEM_COLS = 128;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
-  static constexpr int AUX_BYTES = 1024 + 5 * (kMaxExperts + 1) * 4 + 33 * 4;
-  static constexpr int SMEM_BYTES = RING + AUX_BYTES + 1024;
-  static_assert(STAGE1 % 1024 == 0 && STAGE2 % 1024 == 0, "stage alignment");
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(2 * ACC <= TMEM_COLS, "TMEM columns");
-};
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
+template <bool GLU, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    stream_k_kernel(const __grid_constant__ CUtensorMap tm_x,
-                    const __grid_constant__ CUtensorMap tm_w1,
-                    const __grid_constant__ CUtensorMap tm_w3,
-                    const __grid_constant__ CUtensorMap tm_h,
-                    const __grid_constant__ CUtensorMap tm_w2, const StreamKArgs args) {
-  using C = StreamKCfg;
-  constexpr int BN = C::BN;
+    stream_k_kernel(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_w0,
+                    const __grid_constant__ CUtensorMap tm_w1, const StreamKArgs args) {
+  using C = GemmCfg<true, GLU, kStreamTokens, STAGES>;
+  constexpr int BN = kStreamTokens;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* aux = ring + C::RING;
-  uint64_t* full1 = reinterpret_cast<uint64_t*>(aux);
-  uint64_t* empty1 = full1 + kSkStages1;
-  uint64_t* full2 = empty1 + kSkStages1;
-  uint64_t* empty2 = full2 + kSkStages2;
-  uint64_t* tfull = empty2 + kSkStages2;  // [2]
-  uint64_t* tempty = tfull + 2;           // [2]
-  uint64_t* drain = tempty + 2;           // [1]
+  uint8_t* aux = tiles + STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;       // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_ok = abort_flag + 1;   // [2] wait decisions, alternating by tile
+  int* s_ok = abort_flag + 1;   // [2] wait decisions, alternating by segment
   int* s_last = s_ok + 2;       // last-arriver flag of the current split tile
-  int* s_start1 = reinterpret_cast<int*>(aux + 1024);  // [kMaxExperts + 1] per pass
-  int* s_start2 = s_start1 + kMaxExperts + 1;
-  int* s_act_tiles = s_start2 + kMaxExperts + 1;
+  int* s_tile_start = reinterpret_cast<int*>(aux + 1024);  // [kMaxExperts + 1]
+  int* s_act_tiles = s_tile_start + kMaxExperts + 1;
   int* s_off = s_act_tiles + kMaxExperts + 1;
   int* s_end = s_off + kMaxExperts + 1;
   int* s_scan = s_end + kMaxExperts + 1;
@@ -445,13 +399,9 @@ __global__ void __launch_bounds__(192, 1)
   const int cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSkStages1; ++s) {
-      mbar_init(&full1[s], 1);
-      mbar_init(&empty1[s], 1);
-    }
-    for (int s = 0; s < kSkStages2; ++s) {
-      mbar_init(&full2[s], 1);
-      mbar_init(&empty2[s], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
@@ -461,11 +411,9 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_x);
-    tma_prefetch_desc(&tm_w1);
-    tma_prefetch_desc(&tm_w3);
-    tma_prefetch_desc(&tm_h);
-    tma_prefetch_desc(&tm_w2);
+    tma_prefetch_desc(&tm_act);
+    tma_prefetch_desc(&tm_w0);
+    if (GLU) tma_prefetch_desc(&tm_w1);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
 
@@ -475,187 +423,100 @@ __global__ void __launch_bounds__(192, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  // the two passes share the token tiling (32 grouped rows); their tile lists
-  // differ in the number of weight tiles per expert
-  build_tile_schedule(args.offsets, n, args.rows_total, BN, args.pass[0].w_tiles, s_off, s_end,
-                      s_act_tiles, s_start1, s_scan);
-  build_tile_schedule(args.offsets, n, args.rows_total, BN, args.pass[1].w_tiles, s_off, s_end,
-                      s_act_tiles, s_start2, s_scan);
+  build_tile_schedule(args.offsets, n, args.rows_total, C::ACT_ROWS, args.w_tiles, s_off, s_end,
+                      s_act_tiles, s_tile_start, s_scan);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
 
   const uint32_t tmem_base = *tmem_slot;
+  const int KB = args.k_blocks;
+  const int64_t U = (int64_t)s_tile_start[n] * KB;  // units of the pass
+  auto range_start = [&](int c) -> int64_t { return (int64_t)c * U / G; };
+  const int64_t u0 = range_start(cta), u1 = range_start(cta + 1);
   const WaitCtl wctl{abort_flag, args.err, args.limit_ns};
 
-  // this CTA's unit range [u0, u1) of pass p: unit u = tile * KB + K block
-  auto units = [&](int p) -> int64_t {
-    const int* st = p == 0 ? s_start1 : s_start2;
-    return (int64_t)st[n] * args.pass[p].k_blocks;
-  };
-  auto range_start = [&](int p, int c) -> int64_t { return (int64_t)c * units(p) / G; };
-  auto decode_tile = [&](int p, int t, int& e, int& at, int& wt) {
-    const int* st = p == 0 ? s_start1 : s_start2;
-    e = find_expert(st, n, t);
-    const int local = t - st[e];
+  auto decode_tile = [&](int t, int& e, int& at, int& wt) {
+    e = find_expert(s_tile_start, n, t);
+    const int local = t - s_tile_start[e];
     const int na = s_act_tiles[e];
     wt = local / na;
     at = local - wt * na;
   };
-  // act row and weight row of unit u of pass p
-  auto unit_rows = [&](int p, int64_t u, int& kb, int& act_row, int& w_row) {
-    const int KB = args.pass[p].k_blocks;
-    const int t = (int)(u / KB);
-    kb = (int)(u - (int64_t)t * KB);
-    int e, at, wt;
-    decode_tile(p, t, e, at, wt);
-    act_row = s_off[e] + at * BN;
-    w_row = e * args.pass[p].w_rows_per_expert + wt * 128;
+  // segments of this CTA's range: tile t, K blocks [kb_lo, kb_hi)
+  const int t_first = u0 < u1 ? (int)(u0 / KB) : 0;
+  const int t_stop = u0 < u1 ? (int)((u1 - 1) / KB) + 1 : 0;
+  auto seg_bounds = [&](int t, int& kb_lo, int& kb_hi) {
+    const int64_t base = (int64_t)t * KB;
+    kb_lo = u0 > base ? (int)(u0 - base) : 0;
+    kb_hi = u1 < base + KB ? (int)(u1 - base) : KB;
   };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ---
     if (lane == 0) {
-      bool ok = true;
-      // pass 1: W1 and W3 tiles and 32 token rows per unit
-      const int64_t a0 = range_start(0, cta), a1 = range_start(0, cta + 1);
       int it = 0;
-      for (int64_t u = a0; ok && u < a1; ++u, ++it) {
-        const int s = it % kSkStages1;
-        const uint32_t ph = (uint32_t)(it / kSkStages1) & 1u;
-        if (!mbar_wait(&empty1[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
-          ok = false;
-          break;
-        }
-        int kb, act_row, w_row;
-        unit_rows(0, u, kb, act_row, w_row);
-        uint8_t* stg = ring + s * C::STAGE1;
-        mbar_arrive_expect_tx(&full1[s], C::STAGE1);
-        tma_load_2d(stg, &tm_w1, kb * 64, w_row, &full1[s]);
-        tma_load_2d(stg + C::TILE, &tm_w3, kb * 64, w_row, &full1[s]);
-        tma_load_2d(stg + 2 * C::TILE, &tm_x, kb * 64, act_row, &full1[s]);
-      }
-      // the pass-2 ring overlays the pass-1 ring: every pass-1 slot must have
-      // been read by the MMAs (released) before it is refilled
-      for (int j = (it > kSkStages1 ? it - kSkStages1 : 0); ok && j < it; ++j)
-        ok = mbar_wait(&empty1[j % kSkStages1], (uint32_t)(j / kSkStages1) & 1u, wctl,
-                       kErrTimeoutProducer);
-      // pass 2: the first W2 tiles go out now, their H rows after the grid wait
-      const int64_t b0 = range_start(1, cta), b1 = range_start(1, cta + 1);
-      const int64_t pre = b1 - b0 < kSkStages2 ? b1 - b0 : kSkStages2;
-      int it2 = 0;
-      for (int64_t u = b0; ok && u < b0 + pre; ++u, ++it2) {
-        int kb, act_row, w_row;
-        unit_rows(1, u, kb, act_row, w_row);
-        mbar_arrive_expect_tx(&full2[it2], C::STAGE2);
-        tma_load_2d(ring + it2 * C::STAGE2, &tm_w2, kb * 64, w_row, &full2[it2]);
-      }
-      if (ok) {
-        // wait until every CTA's pass-1 outputs (H, including split tiles
-        // finished by their last contributor) are written
-        bool reached = ld_acquire_gpu(&args.grid_bar[0]) >= (unsigned)G;
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t i = 1; !reached; ++i) {
-          reached = ld_acquire_gpu(&args.grid_bar[0]) >= (unsigned)G;
-          if (!reached && (i & 63u) == 0) {
-            if (*abort_flag) break;
-            if (global_timer_ns() - t0 > args.limit_ns) {
-              atomicOr(args.err, kErrTimeoutProducer);
-              *abort_flag = 1;
-              break;
-            }
+      bool ok = true;
+      for (int t = t_first; ok && t < t_stop; ++t) {
+        int e, at, wt, kb_lo, kb_hi;
+        decode_tile(t, e, at, wt);
+        seg_bounds(t, kb_lo, kb_hi);
+        const int act_row = s_off[e] + at * C::ACT_ROWS;
+        const int w_row = e * args.w_rows_per_expert + wt * C::W_ROWS;
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
+            ok = false;
+            break;
           }
-        }
-        // H was written through the generic proxy; the loads below use the async proxy
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        // the last producer past the wait resets both counters for the next call
-        if (reached && atomicAdd(&args.grid_bar[1], 1u) == (unsigned)G - 1u) {
-          args.grid_bar[0] = 0u;
-          args.grid_bar[1] = 0u;
+          uint8_t* st = tiles + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          const int kx = kb * C::BK;
+          tma_load_2d(st, &tm_w0, kx, w_row, &full[s]);
+          if (GLU) tma_load_2d(st + C::A_BYTES, &tm_w1, kx, w_row, &full[s]);
+          tma_load_2d(st + C::NUM_A * C::A_BYTES, &tm_act, kx, act_row, &full[s]);
         }
       }
-      // the deferred H rows complete the stages already holding their W2 tile
-      // (issued even after a failed wait, so that every stage's bytes land)
-      it2 = 0;
-      for (int64_t u = b0; u < b0 + pre && it2 < (int)pre; ++u, ++it2) {
-        if (!ok) break;
-        int kb, act_row, w_row;
-        unit_rows(1, u, kb, act_row, w_row);
-        tma_load_2d(ring + it2 * C::STAGE2 + C::TILE, &tm_h, kb * 64, act_row, &full2[it2]);
-      }
-      for (int64_t u = b0 + pre; ok && u < b1; ++u, ++it2) {
-        const int s = it2 % kSkStages2;
-        const uint32_t ph = (uint32_t)(it2 / kSkStages2) & 1u;
-        if (!mbar_wait(&empty2[s], ph ^ 1u, wctl, kErrTimeoutProducer)) {
-          ok = false;
-          break;
-        }
-        int kb, act_row, w_row;
-        unit_rows(1, u, kb, act_row, w_row);
-        uint8_t* stg = ring + s * C::STAGE2;
-        mbar_arrive_expect_tx(&full2[s], C::STAGE2);
-        tma_load_2d(stg, &tm_w2, kb * 64, w_row, &full2[s]);
-        tma_load_2d(stg + C::TILE, &tm_h, kb * 64, act_row, &full2[s]);
-      }
-      // let every issued copy land before the CTA can exit
-      for (int j = (it2 > kSkStages2 ? it2 - kSkStages2 : 0); j < it2; ++j)
-        drain_wait(&full2[j % kSkStages2], (uint32_t)(j / kSkStages2) & 1u, args.err,
-                   args.limit_ns);
-      if (it2 == 0)
-        for (int j = (it > kSkStages1 ? it - kSkStages1 : 0); j < it; ++j)
-          drain_wait(&full1[j % kSkStages1], (uint32_t)(j / kSkStages1) & 1u, args.err,
-                     args.limit_ns);
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        drain_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, args.err, args.limit_ns);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer ---
     if (lane == 0) {
-      int lt = 0;
+      int it = 0, lt = 0;
       bool ok = true;
-      for (int p = 0; ok && p < 2; ++p) {
-        const int KB = args.pass[p].k_blocks;
-        const int64_t u0 = range_start(p, cta), u1 = range_start(p, cta + 1);
-        const int nst = p == 0 ? kSkStages1 : kSkStages2;
-        const int sbytes = p == 0 ? C::STAGE1 : C::STAGE2;
-        uint64_t* full = p == 0 ? full1 : full2;
-        uint64_t* empty = p == 0 ? empty1 : empty2;
-        int it = 0;
-        for (int64_t u = u0; ok && u < u1; ++lt) {
-          // one tile: this CTA's units [u, seg_end) of it
-          const int t = (int)(u / KB);
-          const int64_t seg_end = ((int64_t)t + 1) * KB < u1 ? ((int64_t)t + 1) * KB : u1;
-          const int b = lt & 1;
-          const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
-          if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) {
+      for (int t = t_first; ok && t < t_stop; ++t, ++lt) {
+        int kb_lo, kb_hi;
+        seg_bounds(t, kb_lo, kb_hi);
+        const int b = lt & 1;
+        const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(&tempty[b], tph ^ 1u, wctl, kErrTimeoutMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + (uint32_t)(b * C::ACC_COLS);
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t d0 = tmem_base + (uint32_t)(b * C::ACC);
-          for (int64_t v = u; v < seg_end; ++v, ++it) {
-            const int s = it % nst;
-            const uint32_t ph = (uint32_t)(it / nst) & 1u;
-            if (!mbar_wait(&full[s], ph, wctl, kErrTimeoutMma)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t sa = smem_u32(ring + s * sbytes);
-            const uint32_t sb = sa + (p == 0 ? 2 : 1) * C::TILE;
+          const uint32_t sa = smem_u32(tiles + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::NUM_A * C::A_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t accum = (v != u || kk != 0) ? 1u : 0u;
-              mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
-                          C::IDESC, accum);
-              if (p == 0)
-                mma_bf16_ss(d0 + BN, sdesc_kmajor_sw128(sa + C::TILE + kk * 32),
-                            sdesc_kmajor_sw128(sb + kk * 32), C::IDESC, accum);
-            }
-            mma_commit(&empty[s]);
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
+            mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
+                        C::IDESC, accum);
+            if (GLU)
+              mma_bf16_ss(d0 + BN, sdesc_kmajor_sw128(sa + C::A_BYTES + kk * 32),
+                          sdesc_kmajor_sw128(sb + kk * 32), C::IDESC, accum);
           }
-          if (!ok) break;
-          mma_commit(&tfull[b]);
-          u = seg_end;
+          mma_commit(&empty[s]);
         }
+        if (!ok) break;
+        mma_commit(&tfull[b]);
       }
       mma_commit(drain);
       drain_wait(drain, 0, args.err, args.limit_ns);
@@ -665,131 +526,109 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;            // this warp's TMEM lane quarter
     const int et = threadIdx.x - 64;   // 0..127
     const int r = q * 32 + lane;       // accumulator row (weight row inside the tile)
+    auto cta_of_unit = [&](int64_t u) {
+      int c = (int)(u * G / U);
+      while (c + 1 < G && range_start(c + 1) <= u) ++c;
+      while (c > 0 && range_start(c) > u) --c;
+      return c;
+    };
     int lt = 0;
-    bool ok = true;
-    for (int p = 0; ok && p < 2; ++p) {
-      const StreamPass& P = args.pass[p];
-      const int KB = P.k_blocks;
-      const int64_t U = units(p);
-      const int64_t u0 = range_start(p, cta), u1 = range_start(p, cta + 1);
-      auto cta_of_unit = [&](int64_t u) {
-        int c = (int)(u * G / U);
-        while (c + 1 < G && range_start(p, c + 1) <= u) ++c;
-        while (c > 0 && range_start(p, c) > u) --c;
-        return c;
-      };
-      const int t_first = u0 < u1 ? (int)(u0 / KB) : 0;
-      const int t_stop = u0 < u1 ? (int)((u1 - 1) / KB) + 1 : 0;
-      for (int t = t_first; t < t_stop; ++t, ++lt) {
-        const int b = lt & 1;
-        const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
-        // one thread decides for all four warps (they then meet the same barriers);
-        // the decision slot alternates so the next write cannot overtake a read
-        if (et == 0) s_ok[b] = mbar_wait(&tfull[b], tph, wctl, kErrTimeoutEpilogue) ? 1 : 0;
-        named_bar_sync(1, 128);
-        if (!s_ok[b]) {
-          ok = false;
-          break;
+    for (int t = t_first; t < t_stop; ++t, ++lt) {
+      const int b = lt & 1;
+      const uint32_t tph = (uint32_t)(lt >> 1) & 1u;
+      // one thread decides for all four warps (they then meet the same barriers);
+      // the decision slot alternates so the next write cannot overtake a read
+      if (et == 0) s_ok[b] = mbar_wait(&tfull[b], tph, wctl, kErrTimeoutEpilogue) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!s_ok[b]) break;
+      tc_fence_after_sync();
+      int e, at, wt, kb_lo, kb_hi;
+      decode_tile(t, e, at, wt);
+      seg_bounds(t, kb_lo, kb_hi);
+      const int act_row0 = s_off[e] + at * C::ACT_ROWS;
+      const int act_end = s_end[e];
+      const int j = wt * 128 + r;  // output column
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      float acc[C::ACC_COLS];
+#pragma unroll
+      for (int c = 0; c < C::ACC_COLS; c += 32) {
+        float v0[16], v1[16];
+        tmem_ld_2x16(tacc + c, tacc + c + 16, v0, v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          acc[c + i] = v0[i];
+          acc[c + 16 + i] = v1[i];
         }
-        tc_fence_after_sync();
-        int e, at, wt;
-        decode_tile(p, t, e, at, wt);
-        const int64_t base = (int64_t)t * KB;
-        const int kb_lo = u0 > base ? (int)(u0 - base) : 0;
-        const int kb_hi = u1 < base + KB ? (int)(u1 - base) : KB;
-        const int act_row0 = s_off[e] + at * BN;
-        const int act_end = s_end[e];
-        const int j = wt * 128 + r;  // output column
-        const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC);
-        float acc[C::ACC];
-#pragma unroll
-        for (int c = 0; c < C::ACC; c += 32) {
-          float v0[16], v1[16];
-          tmem_ld_2x16(tacc + c, tacc + c + 16, v0, v1);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            acc[c + i] = v0[i];
-            acc[c + 16 + i] = v1[i];
-          }
-        }
-        const int ncols = p == 0 ? C::ACC : BN;  // pass 2 uses the first 32 columns
-        bool emit = (kb_lo == 0 && kb_hi == KB);  // this CTA covers the whole tile
-        if (!emit) {
-          // publish this CTA's slice, then count the arrival
-          const int slot = u0 > base ? 0 : 1;
-          float4* dst = reinterpret_cast<float4*>(
-              args.partials + ((size_t)(cta * 2 + slot) * 128 + r) * kSkPartStride);
-#pragma unroll
-          for (int c = 0; c < C::ACC; c += 4)
-            if (c < ncols) dst[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-          __threadfence();
-          named_bar_sync(1, 128);
-          // contributors: the CTAs from the one holding the tile's first unit to the
-          // one holding its last, skipping those whose range is empty
-          const int c_first = cta_of_unit(base), c_last = cta_of_unit(base + KB - 1);
-          if (et == 0) {
-            int parts = 0;
-            int64_t lo = range_start(p, c_first);
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int64_t hi = range_start(p, cc + 1);
-              parts += hi > lo ? 1 : 0;
-              lo = hi;
-            }
-            const int old = atomicAdd(&args.counters[t], 1);
-            *s_last = (old == parts - 1) ? 1 : 0;
-          }
-          named_bar_sync(1, 128);
-          emit = *s_last != 0;
-          if (emit) {
-            __threadfence();
-            // every contributor's slice, in CTA order
-#pragma unroll
-            for (int c = 0; c < C::ACC; ++c) acc[c] = 0.0f;
-            int64_t lo = range_start(p, c_first);
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int64_t hi = range_start(p, cc + 1);
-              const bool contributes = hi > lo;
-              const int sl = lo > base ? 0 : 1;
-              lo = hi;
-              if (!contributes) continue;
-              const float4* src = reinterpret_cast<const float4*>(
-                  args.partials + ((size_t)(cc * 2 + sl) * 128 + r) * kSkPartStride);
-#pragma unroll
-              for (int c = 0; c < C::ACC; c += 4) {
-                if (c < ncols) {
-                  const float4 v = __ldcg(src + c / 4);
-                  acc[c] += v.x;
-                  acc[c + 1] += v.y;
-                  acc[c + 2] += v.z;
-                  acc[c + 3] += v.w;
-                }
-              }
-            }
-            if (et == 0) args.counters[t] = 0;  // ready for the next pass / call
-          }
-        }
-        if (emit) {
-          // lane <-> weight row j (output column); accumulator columns <-> token rows
-#pragma unroll
-          for (int i = 0; i < BN; ++i) {
-            const int row = act_row0 + i;
-            if (row < act_end) {
-              const float v = p == 0 ? silu_mul(acc[i], acc[BN + i]) : acc[i];
-              const __nv_bfloat16 hv = __float2bfloat16_rn(v);
-              P.out[(size_t)row * P.out_ld + j] = *reinterpret_cast<const uint16_t*>(&hv);
-            }
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
       }
-      if (p == 0 && ok) {
-        // every pass-1 output of this CTA is written: publish it to the grid
+      bool emit = (kb_lo == 0 && kb_hi == KB);  // this CTA covers the whole tile
+      if (!emit) {
+        // publish this CTA's slice, then count the arrival
+        const int64_t base = (int64_t)t * KB;
+        const int slot = u0 > base ? 0 : 1;
+        float4* dst = reinterpret_cast<float4*>(
+            args.partials + ((size_t)(cta * 2 + slot) * 128 + r) * C::ACC_COLS);
+#pragma unroll
+        for (int c = 0; c < C::ACC_COLS; c += 4)
+          dst[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
         __threadfence();
         named_bar_sync(1, 128);
-        if (et == 0) atomicAdd(&args.grid_bar[0], 1u);
+        // contributors: the CTAs from the one holding the tile's first unit to the
+        // one holding its last, skipping those whose range is empty
+        const int c_first = cta_of_unit(base), c_last = cta_of_unit(base + KB - 1);
+        if (et == 0) {
+          int parts = 0;
+          int64_t lo = range_start(c_first);
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            const int64_t hi = range_start(cc + 1);
+            parts += hi > lo ? 1 : 0;
+            lo = hi;
+          }
+          const int old = atomicAdd(&args.counters[t], 1);
+          *s_last = (old == parts - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        emit = *s_last != 0;
+        if (emit) {
+          __threadfence();
+          // every contributor's slice, in CTA order
+#pragma unroll
+          for (int c = 0; c < C::ACC_COLS; ++c) acc[c] = 0.0f;
+          int64_t lo = range_start(c_first);
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            const int64_t hi = range_start(cc + 1);
+            const bool contributes = hi > lo;
+            const int sl = lo > base ? 0 : 1;
+            lo = hi;
+            if (!contributes) continue;
+            const float4* src = reinterpret_cast<const float4*>(
+                args.partials + ((size_t)(cc * 2 + sl) * 128 + r) * C::ACC_COLS);
+#pragma unroll
+            for (int c = 0; c < C::ACC_COLS; c += 4) {
+              const float4 v = __ldcg(src + c / 4);
+              acc[c] += v.x;
+              acc[c + 1] += v.y;
+              acc[c + 2] += v.z;
+              acc[c + 3] += v.w;
+            }
+          }
+          if (et == 0) args.counters[t] = 0;  // ready for the next call
+        }
       }
+      if (emit) {
+        // lane <-> weight row j (output column); accumulator columns <-> token rows
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int row = act_row0 + i;
+          if (row < act_end) {
+            const float v = GLU ? silu_mul(acc[i], acc[BN + i]) : acc[i];
+            const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+            args.out[(size_t)row * args.out_ld + j] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
     }
   }
 
@@ -857,22 +696,22 @@ static cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& w0, const C
   return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
 }
 
-static cudaError_t run_stream_k(const CUtensorMap& x, const CUtensorMap& w1, const CUtensorMap& w3,
-                                const CUtensorMap& h, const CUtensorMap& w2,
-                                const StreamKArgs& args, int grid, cudaStream_t st) {
-  using C = StreamKCfg;
-  cudaError_t e = cudaFuncSetAttribute(stream_k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool GLU, int STAGES>
+static cudaError_t run_stream_k(const CUtensorMap& a, const CUtensorMap& w0,
+                                const CUtensorMap& w1, const StreamKArgs& args, int grid,
+                                cudaStream_t st) {
+  using C = GemmCfg<true, GLU, kStreamTokens, STAGES>;
+  auto kern = stream_k_kernel<GLU, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(stream_k_kernel, dim3(grid), dim3(192), C::SMEM_BYTES, st, x, w1, w3, h, w2,
-                    args);
+  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
 }
 
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
                               const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                               uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
-                              float* partials, int* counters, unsigned* grid_bar,
-                              cudaStream_t st) {
+                              float* partials, int* counters, cudaStream_t st) {
   const int R = s.T * s.top_k;
   if (R == 0) return cudaSuccess;
   const int d = s.dim, hd = s.hidden, n = s.n_experts;
@@ -912,12 +751,15 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
   // c rows has ceil(c / 32) token tiles, so a pass has at most
   // (R / 32 + n) * (weight tiles per expert) tiles
   const int64_t max_tiles = ((int64_t)R / kStreamTokens + n) * ((d > hd ? d : hd) / 128);
-  if (partials != nullptr && counters != nullptr && grid_bar != nullptr &&
-      max_tiles <= kStreamKCounters && grid <= kStreamKMaxCtas) {
-    const StreamKArgs k{offsets, err, kWaitLimitNs, n, R, partials, counters, grid_bar,
-                        {StreamPass{h, d / 64, hd / 128, hd, hd},
-                         StreamPass{y_perm, hd / 64, d / 128, d, d}}};
-    return run_stream_k(tm_x, tm_w1, tm_w3, tm_h, tm_w2, k, grid, st);
+  if (partials != nullptr && counters != nullptr && max_tiles <= kStreamKCounters &&
+      grid <= kStreamKMaxCtas) {
+    const StreamKArgs k1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R,
+                         partials, counters};
+    e = run_stream_k<true, 6>(tm_x, tm_w1, tm_w3, k1, grid, st);
+    if (e != cudaSuccess) return e;
+    const StreamKArgs k2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 128, d, d, R,
+                         partials, counters};
+    return run_stream_k<false, 10>(tm_h, tm_w2, tm_w2, k2, grid, st);
   }
   e = run_gemm<true, true, kStreamTokens, 6>(tm_x, tm_w1, tm_w3, a1, grid, st);
   if (e != cudaSuccess) return e;

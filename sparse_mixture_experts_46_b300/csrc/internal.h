@@ -18,12 +18,10 @@ constexpr int kStreamTokens = 32;        // token chunk (MMA N) of the weight st
 constexpr int kAutoStreamMaxT = 32;      // MOE_FFN_AUTO: weight stream when T <= this
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
-// Workspace control region (zeroed by moe_workspace_init): the error word and,
-// 512 bytes in, the two grid counters of the weight stream's pass boundary in
+// Workspace control region (zeroed by moe_workspace_init): the error word in
 // the first 4 KB, then the per-tile arrival counters of the stream-K weight
-// stream (all left zero by every completed call).
+// stream (left zero by every completed call).
 constexpr size_t kWsHeaderBytes = 4096;
-constexpr size_t kWsGridBarOffset = 512;
 constexpr size_t kWsControlBytes = 65536;
 constexpr int kStreamKCounters = (int)((kWsControlBytes - kWsHeaderBytes) / 4);
 constexpr int kStreamKMaxCtas = 256;  // partial slots are sized for this many CTAs
@@ -31,7 +29,6 @@ constexpr int kStreamKMaxCtas = 256;  // partial slots are sized for this many C
 // Device workspace layout: one header page, then 256-byte aligned arrays.
 struct WsLayout {
   size_t err;          // uint32 error word (header)
-  size_t grid_bar;     // uint32 [2] (header): weight-stream pass boundary
   size_t counters;     // int32 [kStreamKCounters] (control region)
   size_t partials;     // f32 [kStreamKMaxCtas][2][128][64] stream-K accumulator slices
   size_t ids;          // int32 [R]
@@ -100,13 +97,12 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
                            cudaStream_t st);
 // Grouped expert FFN; returns cudaErrorInvalidValue when a tensor map cannot
 // be encoded.
-// partials / counters / grid_bar: the workspace's stream-K regions (null: the
-// weight stream uses whole-tile rounds in two launches).
+// partials / counters: the workspace's stream-K regions (null: the weight
+// stream uses whole-tile rounds).
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
                               const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                               uint16_t* h, uint16_t* y_perm, int path, uint32_t* err,
-                              float* partials, int* counters, unsigned* grid_bar,
-                              cudaStream_t st);
+                              float* partials, int* counters, cudaStream_t st);
 // CTA-pair variant (weights on the MMA M side, cta_group::2); requires
 // pair_ffn_supported(s).
 bool pair_ffn_supported(const moe_shape& s);

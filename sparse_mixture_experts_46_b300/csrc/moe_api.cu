@@ -44,7 +44,6 @@ WsLayout ws_layout(const moe_shape* s) {
   L.nchunks = (int)((R + kPermuteChunk - 1) / kPermuteChunk);
   size_t off = 0;
   L.err = off;
-  L.grid_bar = kWsGridBarOffset;
   L.counters = kWsHeaderBytes;
   off += kWsControlBytes;  // control region: error word, stream-K counters
   auto take = [&](size_t bytes) {
@@ -215,7 +214,7 @@ moe_status moe_expert_ffn_grouped(const moe_shape* shape, const moe_bf16* x_perm
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const cudaError_t e = launch_expert_ffn(*shape, x_perm, offsets, w1, w3, w2, h, y_perm, path,
                                           at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
-                                          at<int>(ws, L.counters), at<unsigned>(ws, L.grid_bar),
+                                          at<int>(ws, L.counters),
                                           static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
@@ -281,7 +280,7 @@ moe_status moe_layer_forward(const moe_shape* shape, const moe_layer_opts* opts,
   e = launch_expert_ffn(*shape, at<uint16_t>(ws, L.x_perm), offsets, w1, w3, w2,
                         at<uint16_t>(ws, L.h), at<uint16_t>(ws, L.y_perm), path,
                         at<uint32_t>(ws, L.err), at<float>(ws, L.partials),
-                        at<int>(ws, L.counters), at<unsigned>(ws, L.grid_bar), st);
+                        at<int>(ws, L.counters), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_combine(*shape, at<uint16_t>(ws, L.y_perm), at<int32_t>(ws, L.slot_row), d_gates,
                      residual, y, st);
