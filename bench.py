@@ -768,7 +768,7 @@ def run_stack_bench(args, rank, world):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import moe_oracle as orc
-        rows = sample_rows(T, 4, 5)
+        rows = sample_rows(T, 2, 5)
         keep = [torch.empty_like(x0) for _ in range(NL)]
         step(keep=keep)
         torch.cuda.synchronize()
