@@ -52,7 +52,11 @@ def layer_inputs(cfg):
     (1, 256, 160, 8), (64, 128, 48, 1), (600, 4096, 160, 8),
     # the wide router splits the model dimension over a cluster of up to 8 CTAs
     # while the token tiles leave SMs idle; 75 tiles (9600 tokens) run unsplit
-    (16, 4096, 160, 8), (9600, 128, 40, 2)])
+    (16, 4096, 160, 8), (9600, 128, 40, 2),
+    # Mixtral's model dimension and half of it: single tokens, fewer tokens
+    # than SMs, fewer than 8 experts, K = n, and 20000 tokens
+    (1, 4096, 8, 2), (16, 4096, 8, 2), (77, 2048, 8, 2), (300, 4096, 5, 3),
+    (129, 4096, 1, 1), (1000, 2048, 8, 8), (20000, 4096, 8, 2), (4097, 2048, 7, 1)])
 def test_router_matches_oracle(T, dim, n, K):
     cfg = mi.Config("r", T=T, dim=dim, hidden=128, n_experts=n, top_k=K, seed=700 + T + n)
     x, wg = layer_inputs(cfg)
@@ -67,6 +71,17 @@ def test_router_exact_ties_go_to_lower_index():
     assert np.all(ids == np.array([0, 1]))
     assert np.all(gates == 0.5)
     assert counts.tolist() == [33, 33, 0, 0, 0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("dim", [128, 4096])
+def test_router_exact_ties_go_to_lower_index_at_dims(dim):
+    # all logits exactly 0, at a small and at Mixtral's model dimension
+    cfg = mi.Config("tie", T=300, dim=dim, hidden=128)
+    x = np.zeros((cfg.T, dim), np.uint16)
+    ids, gates, counts = run_router(cfg, x, mi.gen_router_weight(cfg))
+    assert np.all(ids == np.array([0, 1]))
+    assert np.all(gates == 0.5)
+    assert counts.tolist() == [cfg.T, cfg.T, 0, 0, 0, 0, 0, 0]
 
 
 def test_warp_router_exact_ties_go_to_lower_index():
@@ -87,12 +102,12 @@ def test_wide_router_exact_ties_go_to_lower_index():
     assert counts.tolist() == [cfg.T] * 8 + [0] * 152
 
 
-@pytest.mark.parametrize("n,K", [(8, 2), (24, 2), (40, 4)])
-def test_router_nan_logit_counts_as_minus_infinity(n, K):
+@pytest.mark.parametrize("n,K,dim", [(8, 2, 128), (24, 2, 128), (40, 4, 128), (8, 2, 4096)])
+def test_router_nan_logit_counts_as_minus_infinity(n, K, dim):
     # every token's logit for expert 3 is NaN (a NaN column of W_g): all three
     # routers (tensor-core n <= 16, CUDA-core n <= 32, wide) must route as if
-    # expert 3 did not exist
-    cfg = mi.Config("nan", T=200, dim=128, hidden=128, n_experts=n, top_k=K, seed=900 + n)
+    # expert 3 did not exist, at a small and at Mixtral's model dimension
+    cfg = mi.Config("nan", T=200, dim=dim, hidden=128, n_experts=n, top_k=K, seed=900 + n)
     wg = mi.gen_router_weight(cfg)
     keep = [e for e in range(n) if e != 3]
     wg_rest = np.ascontiguousarray(wg[:, keep])
