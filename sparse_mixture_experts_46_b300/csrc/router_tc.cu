@@ -15,10 +15,11 @@
 //   * one thread issues tcgen05.mma M=128 x N=16 x K=16 into a 16-column fp32
 //     TMEM accumulator (bf16 products are exact, accumulation in fp32);
 //   * when the K range is split over a cluster of `split` CTAs (so that enough
-//     SMs stream x), each CTA parks its partial logits in shared memory and
-//     CTA r sums the partials of tokens [r*128/split, (r+1)*128/split) from all
-//     CTAs of the cluster in rank order (distributed shared memory, a fixed
-//     order: deterministic);
+//     SMs stream x), CTA r selects for tokens [r*128/split, (r+1)*128/split):
+//     every CTA stores its partial logits of those tokens straight into CTA
+//     r's shared memory (distributed shared memory, one slot per source rank),
+//     and after one cluster barrier CTA r sums its slots in rank order (a
+//     fixed order: deterministic) without any remote load;
 //   * one thread per token selects the top K: scanning experts in ascending
 //     order, strictly greater wins, so ties go to the lower index; the gates
 //     are the softmax of the selected logits, accumulated in slot order.
@@ -43,7 +44,7 @@ constexpr int kRtMaxStages = 8;
 constexpr size_t kRtSmemBudget = 200 * 1024;
 constexpr int kRtTileBytes = 128 * 128;  // 128 tokens x 64 bf16
 constexpr int kRtWBytes = 16 * 128;      // 16 expert rows x 64 bf16, per K block
-constexpr int kRtPartStride = 17;        // floats per token row of the partials
+constexpr int kRtPartStride = 20;        // floats per partial row (16-byte rows, no bank conflicts)
 constexpr int kRtMaxKbPerCta = 64;
 constexpr uint32_t kRtIdesc = idesc_bf16_f32(128, 16);
 
@@ -62,10 +63,20 @@ __device__ __forceinline__ void tmem_ld_16(uint32_t ta, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+// Request the 128-byte line holding `p` into L2.  Nothing is read into
+// registers or L1, and L2 is the point of coherence, so the prefetch may be
+// issued before pdl_wait(): a line the predecessor writes afterwards is
+// updated in L2 like any other.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 16-byte store into a cluster peer's shared memory (addr 16-byte aligned).
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b, float c,
+                                                 float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
 // 16-byte load from a cluster peer's shared memory (addr 16-byte aligned).
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
@@ -154,6 +165,11 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   for (int e = tid; e < kMaxExperts; e += kRtThreads) hist[e] = 0;
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_x);
   if (warp == 1) tmem_alloc(tmem_slot, 32);
+  {  // this CTA's W_g rows into L2 while the predecessor finishes
+    const char* w0 = reinterpret_cast<const char*>(wg + (size_t)kb0 * 64 * n);
+    const int bytes = kb_per_cta * 64 * n * 2;
+    for (int o = tid * 128; o < bytes; o += kRtThreads * 128) prefetch_l2(w0 + o);
+  }
 
   pdl_wait();  // x and W_g may be written by the previous kernel
   pdl_launch_dependents();
@@ -274,25 +290,36 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const int t = tile * 128 + r;
     if (ok && t < T) select_topk(lg, n, K, t, ids, gates, h);
   } else {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) part[r * kRtPartStride + e] = lg[e];
-    cluster_sync_all();  // every CTA's partials are visible cluster-wide
+    // token row r belongs to CTA r / per; its partials land in that CTA's
+    // slot (this rank, r % per).  The stores are fire-and-forget; the barrier
+    // (release / acquire at cluster scope) makes them visible, and after it no
+    // CTA touches a peer's shared memory, so none has to wait for the others
+    // before leaving.
     const int per = 128 / split;
+    const uint32_t dst = smem_map_rank(
+        smem_u32(part + ((int)rank * per + r % per) * kRtPartStride), (uint32_t)(r / per));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_cluster_f32x4(dst + 16u * q, lg[4 * q], lg[4 * q + 1], lg[4 * q + 2], lg[4 * q + 3]);
+    cluster_sync_all();
     if (tid < per) {
-      const int rr = (int)rank * per + tid;
       float sum[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) sum[e] = 0.0f;
-      const uint32_t local = smem_u32(part + rr * kRtPartStride);
       for (int c = 0; c < split; ++c) {  // rank order: a fixed summation order
-        const uint32_t a = smem_map_rank(local, (uint32_t)c);
+        const float4* src = reinterpret_cast<const float4*>(part + (c * per + tid) * kRtPartStride);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sum[e] += ld_cluster_f32(a + 4u * e);
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = src[q];
+          sum[4 * q] += v.x;
+          sum[4 * q + 1] += v.y;
+          sum[4 * q + 2] += v.z;
+          sum[4 * q + 3] += v.w;
+        }
       }
-      const int t = tile * 128 + rr;
+      const int t = tile * 128 + (int)rank * per + tid;
       if (t < T && !*abort_flag) select_topk(sum, n, K, t, ids, gates, h);
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its partials
   }
 
   __syncthreads();
