@@ -185,53 +185,49 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 
   // W_g rows [64*kb0, 64*(kb0 + kb_per_cta)) transposed into the MMA's B
   // operand: expert e, feature kk of K block kb at byte
-  //   kb*2048 + e*128 + ((kk/8) ^ (e%8))*16 + (kk%8)*2.
-  // Rows are loaded 8 per thread at a time (all loads in flight), then stored.
-  auto store_row = [&](int i, const uint16_t* w) {
-    const int kb = i >> 6, kk = i & 63;
-    uint8_t* base = bw + (size_t)kb * kRtWBytes + (kk & 7) * 2;
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      *reinterpret_cast<uint16_t*>(base + e * 128 + ((((kk >> 3) ^ (e & 7))) << 4)) = w[e];
-  };
+  //   kb*2048 + e*128 + ((kk/8) ^ (e%8))*16 + (kk%8)*2,
+  // so the 8 features kk..kk+7 (kk a multiple of 8) of one expert are one
+  // 16-byte vector.
   const int rows = kb_per_cta * 64;
   if (n == 8 || n == 16) {
-    for (int i0 = tid; i0 < rows; i0 += 8 * kRtThreads) {
+    // a thread takes 8 consecutive rows (its loads all in flight), transposes
+    // them in registers and writes one 16-byte vector per expert
+    for (int g = tid; g < rows / 8; g += kRtThreads) {
+      const int i = g * 8;
       uint4 v[8][2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j * kRtThreads;
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int q = 0; q < 2; ++q)
-          v[j][q] = (i < rows && q * 8 < n)
-                        ? __ldg(reinterpret_cast<const uint4*>(wg + (size_t)(kb0 * 64 + i) * n) + q)
-                        : make_uint4(0u, 0u, 0u, 0u);
-      }
+          v[j][q] = q * 8 < n ? __ldg(reinterpret_cast<const uint4*>(wg + (size_t)(kb0 * 64 + i + j) * n) + q)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      uint8_t* base = bw + (size_t)(i >> 6) * kRtWBytes;
+      const int chunk = (i & 63) >> 3;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j * kRtThreads;
-        if (i < rows) {
-          uint16_t w[16];
+      for (int e = 0; e < 16; ++e) {
+        uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t u[4] = {v[j][q].x, v[j][q].y, v[j][q].z, v[j][q].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              w[q * 8 + 2 * h] = (uint16_t)(u[h] & 0xFFFFu);
-              w[q * 8 + 2 * h + 1] = (uint16_t)(u[h] >> 16);
-            }
-          }
-          store_row(i, w);
+        for (int p = 0; p < 4; ++p) {
+          const uint4 a = v[2 * p][e >> 3], b = v[2 * p + 1][e >> 3];
+          const uint32_t wa = ((e & 7) >> 1) == 0 ? a.x : ((e & 7) >> 1) == 1 ? a.y : ((e & 7) >> 1) == 2 ? a.z : a.w;
+          const uint32_t wb = ((e & 7) >> 1) == 0 ? b.x : ((e & 7) >> 1) == 1 ? b.y : ((e & 7) >> 1) == 2 ? b.z : b.w;
+          const uint32_t lo = (e & 1) ? (wa >> 16) : (wa & 0xFFFFu);
+          const uint32_t hi = (e & 1) ? (wb >> 16) : (wb & 0xFFFFu);
+          w[p] = lo | (hi << 16);
         }
+        *reinterpret_cast<uint4*>(base + e * 128 + ((chunk ^ (e & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   } else {
     for (int i = tid; i < rows; i += kRtThreads) {
       const int k = kb0 * 64 + i;
-      uint16_t w[16];
+      const int kb = i >> 6, kk = i & 63;
+      uint8_t* base = bw + (size_t)kb * kRtWBytes + (kk & 7) * 2;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = e < n ? __ldg(wg + (size_t)k * n + e) : (uint16_t)0;
-      store_row(i, w);
+      for (int e = 0; e < 16; ++e)
+        *reinterpret_cast<uint16_t*>(base + e * 128 + ((((kk >> 3) ^ (e & 7))) << 4)) =
+            e < n ? __ldg(wg + (size_t)k * n + e) : (uint16_t)0;
     }
   }
   // the generic-proxy writes above are read by the tensor core (async proxy)
