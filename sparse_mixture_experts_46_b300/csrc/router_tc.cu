@@ -17,9 +17,11 @@
 //   * when the K range is split over a cluster of `split` CTAs (so that enough
 //     SMs stream x), CTA r selects for tokens [r*128/split, (r+1)*128/split):
 //     every CTA stores its partial logits of those tokens straight into CTA
-//     r's shared memory (distributed shared memory, one slot per source rank),
-//     and after one cluster barrier CTA r sums its slots in rank order (a
-//     fixed order: deterministic) without any remote load;
+//     r's shared memory (distributed shared memory, one slot per source rank;
+//     the first store waits only for the cluster-barrier phase that every CTA
+//     arrives at when it starts), and after one full cluster barrier CTA r sums
+//     its slots in rank order (a fixed order: deterministic) without any
+//     remote load;
 //   * one thread per token selects the top K: scanning experts in ascending
 //     order, strictly greater wins, so ties go to the lower index; the gates
 //     are the softmax of the selected logits, accumulated in slot order.
@@ -40,8 +42,8 @@ __device__ uint32_t g_router_err = 0;
 namespace {
 
 constexpr int kRtThreads = 128;
-constexpr int kRtMaxStages = 8;
-constexpr size_t kRtSmemBudget = 200 * 1024;
+constexpr int kRtMaxStages = 12;
+constexpr size_t kRtSmemBudget = 227 * 1024;
 constexpr int kRtTileBytes = 128 * 128;  // 128 tokens x 64 bf16
 constexpr int kRtWBytes = 16 * 128;      // 16 expert rows x 64 bf16, per K block
 constexpr int kRtPartStride = 20;        // floats per partial row (16-byte rows, no bank conflicts)
@@ -71,6 +73,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// The two halves of a cluster barrier: arrive without ordering any memory
+// access (it only announces that this CTA is running), and wait with acquire
+// semantics.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // 16-byte store into a cluster peer's shared memory (addr 16-byte aligned).
 __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b, float c,
                                                  float d) {
@@ -151,6 +162,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const uint32_t rank = split > 1 ? cluster_ctarank() : 0u;
   const int tile = blockIdx.x / split;
   const int kb0 = (int)rank * kb_per_cta;
+  // this CTA is running: peers may store into its partial buffer once they
+  // have waited on this phase (just before their first remote store)
+  if (split > 1) cluster_arrive_relaxed();
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -234,7 +248,6 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before_sync();
   __syncthreads();
-  if (split > 1) cluster_sync_all();  // peers' barriers and partial buffers exist
   tc_fence_after_sync();
 
   const uint32_t tmem = *tmem_slot;
@@ -292,6 +305,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     // CTA touches a peer's shared memory, so none has to wait for the others
     // before leaving.
     const int per = 128 / split;
+    cluster_wait();  // every peer of the cluster is running
     const uint32_t dst = smem_map_rank(
         smem_u32(part + ((int)rank * per + r % per) * kRtPartStride), (uint32_t)(r / per));
 #pragma unroll
@@ -428,7 +442,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
-  if (split > 1) cluster_sync_all();  // every peer is running before any DSMEM access
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wctl{abort_flag, err, limit_ns};
@@ -487,7 +500,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   const int per = 128 / split;  // token rows this CTA selects for
   const int row0 = (int)rank * per;
   if (split > 1) {
-    cluster_sync_all();  // every CTA's partials are visible cluster-wide
+    // every CTA's partials are visible cluster-wide (and every peer, having
+    // arrived here, is running)
+    cluster_sync_all();
     // this CTA's token rows: the sum over the cluster in rank order, written
     // back over its own rows (no peer reads them); one item = 4 experts of a
     // row, every peer's 16 bytes requested before the sum
