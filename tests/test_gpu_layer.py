@@ -179,11 +179,13 @@ def test_mixtral_8x22b_dims(path):
 
 @pytest.mark.parametrize("T,dim,n,K", [
     (1, 128, 8, 2), (32, 128, 8, 2), (17, 256, 8, 8), (9, 384, 5, 3), (32, 512, 1, 1),
-    (20, 128, 8, 1), (31, 4096, 8, 2), (12, 6144, 6, 2)])
+    (20, 128, 8, 1), (31, 4096, 8, 2), (12, 6144, 6, 2), (7, 6144, 8, 2), (32, 256, 8, 8)])
 def test_decode_sized_layer_routed_in_one_launch(T, dim, n, K):
     # moe_layer_forward routes, groups and gathers a batch of T <= 32 tokens
     # over n <= 8 experts in one launch: edge batches (1 token, 32 tokens),
-    # K = 1, K = n, fewer than 8 experts, 8x22B's model dimension
+    # K = 1, K = n, fewer than 8 experts, 8x22B's model dimension (with 8
+    # experts, a lane's 16-byte slices of W_g come in an odd count), and the
+    # most assignments the launch takes (32 x 8)
     cfg = mi.Config("small-route", T=T, dim=dim, hidden=256, n_experts=n, top_k=K,
                     seed=46600 + T * 7 + dim + n)
     assert fused_routes_in_one_launch(cfg)
