@@ -36,6 +36,8 @@
 // word, lets its in-flight TMA copies and MMAs land, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "device.cuh"
@@ -364,7 +366,17 @@ struct StreamKArgs {
   int rows_total;          // R
   float* partials;         // [gridDim][2][128][ACC_COLS] fp32 accumulator slices
   int* counters;           // [tiles] arrivals per split tile; zero on entry and exit
+  int presumed_units;      // units of the presumed schedule requested into L2 before
+                           // the dependency wait (0: none)
 };
+
+// L2 prefetch of the box at (x, y) of a tiled tensor map.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 
 template <bool GLU, int STAGES>
 __global__ void __launch_bounds__(192, 1)
@@ -414,6 +426,28 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tm_act);
     tma_prefetch_desc(&tm_w0);
     if (GLU) tma_prefetch_desc(&tm_w1);
+    // The weights do not depend on the kernel that runs before this pass
+    // (the routing before pass 1, pass 1 before pass 2), so the stream can
+    // start while it finishes: the first units of this CTA's range under the
+    // presumed schedule -- every expert touched, with one activation tile
+    // (true whenever T <= 32) -- are requested into L2.
+    // A prefetch is only a hint: a wrong presumption costs the bandwidth of
+    // lines nobody reads, never a wrong result, and L2 is the point of
+    // coherence, so nothing stale can be read.
+    if (args.presumed_units > 0) {
+      const int64_t Up = (int64_t)n * args.w_tiles * args.k_blocks;
+      const int64_t p0 = (int64_t)cta * Up / G;
+      int64_t p1 = (int64_t)(cta + 1) * Up / G;
+      if (p1 > p0 + args.presumed_units) p1 = p0 + args.presumed_units;
+      for (int64_t u = p0; u < p1; ++u) {
+        const int t = (int)(u / args.k_blocks);
+        const int kb = (int)(u - (int64_t)t * args.k_blocks);
+        const int e = t / args.w_tiles, wt = t - e * args.w_tiles;
+        const int w_row = e * args.w_rows_per_expert + wt * C::W_ROWS;
+        tma_prefetch_l2_2d(&tm_w0, kb * C::BK, w_row);
+        if (GLU) tma_prefetch_l2_2d(&tm_w1, kb * C::BK, w_row);
+      }
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
 
@@ -696,6 +730,11 @@ static cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& w0, const C
   return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, a, w0, w1, args);
 }
 
+// Units of a pass each CTA requests into L2 before the dependency wait (24
+// units are 768 KB per CTA in pass 1, 384 KB in pass 2; 48 measured slower,
+// 6 and 12 gained less).
+constexpr int kPresumedUnits = 24;
+
 template <bool GLU, int STAGES>
 static cudaError_t run_stream_k(const CUtensorMap& a, const CUtensorMap& w0,
                                 const CUtensorMap& w1, const StreamKArgs& args, int grid,
@@ -753,12 +792,19 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
   const int64_t max_tiles = ((int64_t)R / kStreamTokens + n) * ((d > hd ? d : hd) / 128);
   if (partials != nullptr && counters != nullptr && max_tiles <= kStreamKCounters &&
       grid <= kStreamKMaxCtas) {
+    // Before pass 1 the HBM idles while the routing finishes, before pass 2
+    // while the last CTAs of pass 1 finish; each pass then starts streaming
+    // its first units by presuming every expert touched (see the kernel).  Only where that presumption nearly always holds: with T tokens
+    // choosing K of n experts uniformly, an expert stays untouched with
+    // probability (1 - K/n)^T (Mixtral decode, T=16: 0.01; 8 of 160: 0.44).
+    const bool presume =
+        s.T <= kStreamTokens && std::pow(1.0 - (double)s.top_k / n, (double)s.T) <= 0.05;
     const StreamKArgs k1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R,
-                         partials, counters};
+                         partials, counters, presume ? kPresumedUnits : 0};
     e = run_stream_k<true, 6>(tm_x, tm_w1, tm_w3, k1, grid, st);
     if (e != cudaSuccess) return e;
     const StreamKArgs k2{offsets, y_perm, err, kWaitLimitNs, n, hd / 64, d / 128, d, d, R,
-                         partials, counters};
+                         partials, counters, presume ? kPresumedUnits : 0};
     return run_stream_k<false, 10>(tm_h, tm_w2, tm_w2, k2, grid, st);
   }
   e = run_gemm<true, true, kStreamTokens, 6>(tm_x, tm_w1, tm_w3, a1, grid, st);
