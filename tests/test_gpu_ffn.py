@@ -95,6 +95,16 @@ def test_ffn_single_row(path):
     check_ffn([0, 0, 1], 128, 128, path, seed=5)
 
 
+@pytest.mark.parametrize("counts", [[4] * 8, [0, 5, 0, 11, 0, 0, 16, 0]])
+def test_stream_presumed_schedule_prefetch(counts):
+    # T = 32 rows over 8 experts with K = 1: (7/8)^32 < 0.05, so each pass of
+    # the weight stream requests the first units of the schedule it presumes
+    # (every expert touched once) into L2 before its dependency wait; the
+    # second case leaves 5 of the 8 experts empty, so the presumption is
+    # wrong and only the results show whether the real schedule was followed
+    check_ffn(counts, 256, 256, "stream", seed=7)
+
+
 def test_ffn_paths_agree_bitwise_structure():
     """Both layouts compute the same rows (values within tolerance of each other)."""
     cfg, x_perm, offsets, w1, w3, w2 = ffn_case([17, 33, 0, 64], 256, 256, 6)
