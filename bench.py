@@ -254,13 +254,14 @@ class E2E:
 
 # Kernels of ours launched per layer call (moe_layer_forward): routing (one
 # launch for a decode-sized batch of T <= 32 tokens over n <= 8 experts; else
-# router, grouping -- one kernel up to 2048 assignments, histogram / scan /
-# scatter above -- and gather), gate/up GEMM, down GEMM, combine.
+# router, grouping -- one kernel up to 8192 assignments (one block, or one
+# cluster above 2048), histogram / scan / scatter above -- and gather),
+# gate/up GEMM, down GEMM, combine.
 def kernels_per_layer(cfg):
     if cfg.T <= 32 and cfg.n_experts <= 8 and cfg.rmsnorm_eps == 0:
         routing = 1
     else:
-        routing = 1 + (3 if cfg.T * cfg.top_k > 2048 else 1) + 1
+        routing = 1 + (3 if cfg.T * cfg.top_k > 8192 else 1) + 1
     return routing + 2 + 1
 
 

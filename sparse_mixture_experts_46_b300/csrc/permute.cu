@@ -14,7 +14,9 @@
 //               writing slot_row[a] and perm_src[row];
 //   4. gather:  x_perm[row] = x[perm_src[row]], 16-byte vector moves, one
 //               thread per slice.
-// For small T*K (decode batches) steps 1-3 run as one single-block kernel.
+// For small T*K (decode batches) steps 1-3 run as one single-block kernel, and
+// up to 8192 assignments (a Mixtral prefill batch of 4096 tokens) as one
+// cluster of up to 8 blocks.
 // With pad > 1 every expert's group starts on a multiple of `pad` rows
 // (offsets are then the padded starts and the group of e ends at
 // offsets[e] + counts[e]); the padding rows get perm_src = -1 and are written
@@ -211,6 +213,87 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   }
 }
 
+// Steps 1-3 for kSmallPermute < T*K <= kClusterPermute, pad == 1: one cluster
+// of ceil(T*K / 1024) blocks, one assignment per thread (block r takes the
+// slice [1024 r, 1024 (r+1))).  Each block counts its slice's experts (warp
+// match + popcount) and stores the counts into slot r of EVERY block's shared
+// memory (distributed shared memory); after the launch's one full cluster
+// barrier each block derives on its own the expert totals, the offsets (their
+// exclusive prefix) and where its slice starts inside every expert group (the
+// slices before it, in rank order), then ranks its assignments -- the same
+// stable order as the other paths.  Block 0 writes counts and offsets.
+constexpr int kClusterPermuteCtas = 8;
+constexpr int kClusterPermute = kClusterPermuteCtas * 1024;
+
+__device__ __forceinline__ void st_cluster_s32p(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(1024) permute_cluster_kernel(const int32_t* __restrict__ ids,
+                                                              int R, int K, int n,
+                                                              int32_t* __restrict__ counts,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ perm_src,
+                                                              int32_t* __restrict__ slot_row) {
+  __shared__ int s_wcnt[32][kMaxExperts];
+  __shared__ int s_slice[kClusterPermuteCtas][kMaxExperts];  // each block's counts
+  __shared__ int s_base[kMaxExperts];
+  __shared__ int s_scan[33];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int nct = (int)gridDim.x;  // the whole grid is one cluster
+  // this block is running: peers may store into it once they have waited on
+  // this phase (just before their first remote store)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();
+  const int a = (int)rank * 1024 + tid;
+  int e = (a < R) ? ids[a] : -1;
+  if ((unsigned)e >= (unsigned)n) e = -1;  // ids outside [0, n) are ignored
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned lower = peers & ((1u << lane) - 1u);
+  if (e >= 0 && lower == 0) s_wcnt[warp][e] = __popc(peers);
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every block is running
+  if (tid < n) {
+    int c = 0;
+    for (int w = 0; w < 32; ++w) c += s_wcnt[w][tid];
+    const uint32_t local = smem_u32(&s_slice[rank][tid]);
+    for (int q = 0; q < nct; ++q) st_cluster_s32p(smem_map_rank(local, (uint32_t)q), c);
+  }
+  cluster_sync_all();  // every block's counts everywhere; no remote access after this
+  int total = 0, before = 0;
+  if (tid < n) {
+    for (int q = 0; q < nct; ++q) {
+      const int v = s_slice[q][tid];
+      total += v;
+      if (q < (int)rank) before += v;
+    }
+  }
+  int all = 0;
+  const int excl = block_exclusive_scan(total, s_scan, &all);
+  if (tid < n) {
+    s_base[tid] = excl + before;
+    if (rank == 0) {
+      offsets[tid] = excl;
+      if (counts) counts[tid] = total;
+    }
+  }
+  if (rank == 0 && tid == 0) offsets[n] = all;
+  __syncthreads();
+  if (e >= 0) {
+    int bw = 0;
+    for (int w = 0; w < warp; ++w) bw += s_wcnt[w][e];
+    const int row = s_base[e] + bw + __popc(lower);
+    slot_row[a] = row;
+    perm_src[row] = a / K;
+  }
+}
+
 cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            int32_t* counts_out, int32_t* offsets, int32_t* chunk_hist,
                            int32_t* chunk_base, int32_t* perm_src, int32_t* slot_row,
@@ -224,6 +307,25 @@ cudaError_t launch_permute(const moe_shape& s, const uint16_t* x, const int32_t*
   if (R <= kSmallPermute) {
     e = launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, st, ids, R, s.top_k, s.n_experts,
                    pad, counts_out, offsets, perm_src, slot_row);
+    if (e != cudaSuccess) return e;
+  } else if (R <= kClusterPermute && pad == 1) {
+    const int nct = (R + 1023) / 1024;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nct);
+    cfg.blockDim = dim3(1024);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nct;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, permute_cluster_kernel, ids, R, s.top_k, s.n_experts, counts_out,
+                           offsets, perm_src, slot_row);
     if (e != cudaSuccess) return e;
   } else {
     e = launch_pdl(permute_hist_kernel, dim3(nchunks), dim3(kPermuteChunk), 0, st, ids, R,

@@ -46,9 +46,13 @@ def random_ids(rng, T, n, K, weights=None):
     return out
 
 
+# the grouping runs as one block up to 2048 assignments, one cluster up to
+# 8192 (2049, 4096 + 2, 8192 below), and histogram / scan / scatter above
 @pytest.mark.parametrize("T,n,K", [(1, 8, 2), (64, 8, 2), (129, 8, 2), (1000, 8, 2),
                                    (3000, 8, 2), (257, 1, 1), (300, 8, 8), (555, 32, 3),
-                                   (100, 64, 6), (300, 256, 8), (2000, 160, 8), (5, 160, 8)])
+                                   (100, 64, 6), (300, 256, 8), (2000, 160, 8), (5, 160, 8),
+                                   (2049, 8, 1), (2049, 8, 2), (4096, 8, 2), (4097, 8, 2),
+                                   (1024, 256, 8), (2730, 7, 3)])
 def test_permute_matches_counting_sort(T, n, K):
     rng = np.random.default_rng(T * 31 + n)
     cfg = mi.Config("p", T=T, dim=128, hidden=128, n_experts=n, top_k=K, seed=900 + T)
@@ -67,6 +71,13 @@ def test_permute_skewed_and_empty_experts():
 def test_permute_all_tokens_one_expert():
     cfg = mi.Config("p", T=700, dim=128, hidden=128, n_experts=4, top_k=1, seed=78)
     ids = np.full((700, 1), 2, np.int32)
+    check_permute(cfg, mi.gen_x(cfg), ids)
+
+
+def test_permute_all_assignments_one_expert_one_cluster():
+    # 8192 assignments (the most the one-cluster grouping takes), all to expert 3
+    cfg = mi.Config("p", T=8192, dim=128, hidden=128, n_experts=4, top_k=1, seed=79)
+    ids = np.full((8192, 1), 3, np.int32)
     check_permute(cfg, mi.gen_x(cfg), ids)
 
 
