@@ -45,14 +45,14 @@ def _check_same(cfg, x, ids):
 
 
 def test_noalloc_grouping_equals_workspace_grouping_twice():
-    # two calls in a row, both above the 2048 assignments that a single block
-    # groups on its own, so both go through the shared scratch tables: the
-    # first with the larger table (24 chunks x 16 experts), the second with a
-    # smaller one (12 chunks x 8 experts) that must not depend on what the
-    # first call left in the scratch
-    for T, n, K, dim, seed in [(3000, 16, 2, 256, 11), (1500, 8, 2, 128, 12)]:
+    # two calls in a row, both above the 8192 assignments that one block or
+    # one cluster groups on its own, so both go through the shared scratch
+    # tables: the first with the larger table (40 chunks x 16 experts), the
+    # second with a smaller one (36 chunks x 8 experts) that must not depend
+    # on what the first call left in the scratch
+    for T, n, K, dim, seed in [(5000, 16, 2, 256, 11), (4500, 8, 2, 128, 12)]:
         R = T * K
-        assert R > 2048
+        assert R > 8192
         _check_same(*_case(T, n, K, dim, seed))
 
 
