@@ -200,10 +200,13 @@ class Buffers:
 
 
 class E2E:
-    """Host -> device -> host loop: every step uploads x from pinned host memory,
-    runs moe_layer_forward and downloads y into pinned host memory.  Uploads and
-    downloads run on their own streams with double-buffered device tensors, so
-    step k+1's upload and step k's download overlap step k's compute."""
+    """Host -> device -> host loop: every step uploads each layer's x from pinned
+    host memory, runs moe_layer_forward for every layer and downloads each y into
+    pinned host memory.  Uploads and downloads run on their own streams with
+    double-buffered device tensors, so step k+1's uploads and step k's downloads
+    overlap step k's compute.  The compute stream meets the copy streams once per
+    step (before its first layer, and one event after its last), so the layers
+    of a step follow one another with nothing between their launches."""
 
     def __init__(self, bufs, compute):
         import torch
@@ -211,14 +214,15 @@ class E2E:
         self.compute = compute
         self.h2d = torch.cuda.Stream()
         self.d2h = torch.cuda.Stream()
-        self.slots = {}
-        for name, b in bufs.items():
-            self.slots[name] = [
-                dict(x=torch.empty_like(b.x), y=torch.empty_like(b.y),
-                     y_host=torch.empty(tuple(b.y.shape), dtype=b.y.dtype).pin_memory(),
-                     up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event(),
-                     used=False)
-                for _ in range(2)]
+        self.slots = []
+        for _ in range(2):
+            self.slots.append(dict(
+                x={n: torch.empty_like(b.x) for n, b in bufs.items()},
+                y={n: torch.empty_like(b.y) for n, b in bufs.items()},
+                y_host={n: torch.empty(tuple(b.y.shape), dtype=b.y.dtype).pin_memory()
+                        for n, b in bufs.items()},
+                up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event(),
+                used=False))
 
     def begin(self, start_event):
         self.h2d.wait_event(start_event)
@@ -227,29 +231,31 @@ class E2E:
     def step(self, k):
         import torch
         import sparse_mixture_experts_46_b300 as moe
+        s = self.slots[k & 1]
+        if s["used"]:
+            self.h2d.wait_event(s["done"])       # the last readers of s["x"] finished
+        with torch.cuda.stream(self.h2d):
+            for name, b in self.bufs.items():
+                s["x"][name].copy_(b.x_host, non_blocking=True)
+        s["up"].record(self.h2d)
+        self.compute.wait_event(s["up"])
+        if s["used"]:
+            self.compute.wait_event(s["down"])   # the last ys in s["y"] were downloaded
         for name, b in self.bufs.items():
-            s = self.slots[name][k & 1]
-            if s["used"]:
-                self.h2d.wait_event(s["done"])       # the last reader of s["x"] finished
-                self.compute.wait_event(s["down"])   # the last y in s["y"] was downloaded
-            with torch.cuda.stream(self.h2d):
-                s["x"].copy_(b.x_host, non_blocking=True)
-            s["up"].record(self.h2d)
-            self.compute.wait_event(s["up"])
-            moe.moe_layer_forward(b.cfg, s["x"], b.wg, b.w1, b.w3, b.w2, s["y"], b.ws,
-                                  stream=self.compute)
-            s["done"].record(self.compute)
-            self.d2h.wait_event(s["done"])
-            with torch.cuda.stream(self.d2h):
-                s["y_host"].copy_(s["y"], non_blocking=True)
-            s["down"].record(self.d2h)
-            s["used"] = True
+            moe.moe_layer_forward(b.cfg, s["x"][name], b.wg, b.w1, b.w3, b.w2, s["y"][name],
+                                  b.ws, stream=self.compute)
+        s["done"].record(self.compute)
+        self.d2h.wait_event(s["done"])
+        with torch.cuda.stream(self.d2h):
+            for name in self.bufs:
+                s["y_host"][name].copy_(s["y"][name], non_blocking=True)
+        s["down"].record(self.d2h)
+        s["used"] = True
 
     def finish(self):
-        for slots in self.slots.values():
-            for s in slots:
-                if s["used"]:
-                    self.compute.wait_event(s["down"])
+        for s in self.slots:
+            if s["used"]:
+                self.compute.wait_event(s["down"])
 
 
 # Kernels of ours launched per layer call (moe_layer_forward): routing (one
