@@ -102,11 +102,13 @@ def test_clock_record_keeps_only_samples_inside_the_timed_window():
     assert empty["samples"] == 0 and empty["sm_mhz"] is None
 
 
-def test_reference_sample_sizes_keep_the_run_bounded():
-    for steps, warmup in [(1, 0), (3, 1), (30, 3), (400, 10), (5000, 10)]:
-        d, p = bench.reference_sample_sizes(steps, warmup)
-        assert d >= 1 and p >= 1 and 2 <= d + p <= 48
-        # the whole run stays near 720 oracle tokens, or 2 per step at most
-        assert (d + p) * (steps + warmup) <= max(720 + 48, 2 * (steps + warmup))
-    assert bench.reference_sample_sizes(3, 1) == (16, 32)
-    assert bench.reference_sample_sizes(400, 10) == (1, 1)
+def test_reference_plan_keeps_the_run_bounded():
+    for steps, warmup in [(1, 0), (3, 1), (20, 5), (30, 3), (400, 10), (5000, 10)]:
+        every, d, p = bench.reference_plan(steps, warmup)
+        assert every >= 1 and d >= 1 and p >= 1 and 2 <= d + p <= 48
+        calls = len(range(0, steps + warmup, every))
+        # at most 20 oracle calls, about 720 tokens in all
+        assert calls <= 20
+        assert (d + p) * calls <= 720 + 48
+    assert bench.reference_plan(3, 1) == (1, 16, 32)
+    assert bench.reference_plan(400, 10) == (21, 12, 24)
