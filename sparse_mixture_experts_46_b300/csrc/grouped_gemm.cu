@@ -794,9 +794,10 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x_perm, const 
       grid <= kStreamKMaxCtas) {
     // Before pass 1 the HBM idles while the routing finishes, before pass 2
     // while the last CTAs of pass 1 finish; each pass then starts streaming
-    // its first units by presuming every expert touched (see the kernel).  Only where that presumption nearly always holds: with T tokens
-    // choosing K of n experts uniformly, an expert stays untouched with
-    // probability (1 - K/n)^T (Mixtral decode, T=16: 0.01; 8 of 160: 0.44).
+    // its first units by presuming every expert touched (see the kernel).
+    // Only where that presumption nearly always holds: with T tokens choosing
+    // K of n experts uniformly, an expert stays untouched with probability
+    // (1 - K/n)^T (Mixtral decode, T=16: 0.01; 8 of 160: 0.44).
     const bool presume =
         s.T <= kStreamTokens && std::pow(1.0 - (double)s.top_k / n, (double)s.T) <= 0.05;
     const StreamKArgs k1{offsets, h, err, kWaitLimitNs, n, d / 64, hd / 128, hd, hd, R,
