@@ -419,6 +419,47 @@ def ffn_roofline(ffn, pk, pk_kind, traffic, clk=None):
             "unit": "GB/s", "frac": t_hbm, "traffic": traffic, "peak_kind": pk_kind + " copy"}
 
 
+def cublas_same_clocks(b, cfg, rounds=4, calls=5):
+    """The batch's expert FFN next to cuBLAS GEMMs of the same FLOPs (bf16
+    [R, d] x [d, 2h] and [R, h] x [h, d], fp32 accumulation), in alternating
+    rounds so that both run at the same clocks: median TFLOP/s of each and
+    their ratio.  A check of the kernel against the vendor library on the same
+    shapes, beside the roofline's measured peak (cuBLAS 8192^3)."""
+    import torch
+    R, d, h = cfg.T * cfg.top_k, cfg.dim, cfg.hidden
+    g = torch.Generator(device="cuda").manual_seed(46)
+    X = torch.randn((R, d), device="cuda", generator=g).to(torch.bfloat16)
+    W13 = (torch.randn((d, 2 * h), device="cuda", generator=g) * 0.01).to(torch.bfloat16)
+    H = torch.randn((R, h), device="cuda", generator=g).to(torch.bfloat16)
+    W2 = (torch.randn((h, d), device="cuda", generator=g) * 0.01).to(torch.bfloat16)
+    flop = 6.0 * R * d * h
+
+    def library():
+        torch.matmul(X, W13)
+        torch.matmul(H, W2)
+
+    arms = {"ours": b.ffn, "cublas": library}
+    for f in arms.values():
+        f()
+    torch.cuda.synchronize()
+    res = {k: [] for k in arms}
+    for r in range(rounds):
+        for name in (list(arms) if r % 2 == 0 else list(arms)[::-1]):
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(calls):
+                arms[name]()
+            e.record()
+            torch.cuda.synchronize()
+            res[name].append(flop / (a.elapsed_time(e) / calls * 1e-3) / 1e12)
+    ours, lib = float(np.median(res["ours"])), float(np.median(res["cublas"]))
+    del X, W13, H, W2
+    return {"ours_tflops": ours, "cublas_tflops": lib, "ratio": ours / lib,
+            "cublas_gemms": "[%d, %d] x [%d, %d] and [%d, %d] x [%d, %d], bf16"
+                            % (R, d, d, 2 * h, R, h, h, d),
+            "rounds": rounds, "calls_per_round": calls}
+
+
 # ------------------------------------------------------------ oracle CPU ---
 
 def cpu_cores():
@@ -1005,6 +1046,9 @@ def run_layers_bench(args, rank, world):
         "gpu_launches": args.steps * sum(kernels_per_layer(layers[r][0]) for r in roles),
         "clocks": clk,
     }
+    if result["roofline"]["bound"] == "tensor":
+        result["roofline"]["same_clocks_cublas"] = cublas_same_clocks(bufs[main_role], main_cfg)
+        check_device("after the cuBLAS comparison")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import moe_oracle as orc
         counts = {r: (None if layers[r][0].T <= 16 else (32 if len(roles) > 1 else 64))
