@@ -129,8 +129,9 @@ MOE_API moe_status moe_router_topk(const moe_shape* shape, const moe_bf16* x,
  *   grouped row), x_perm [T*K, dim] (x_perm[r] = x[perm_src[r]], bit copy).
  *   ws: workspace of moe_workspace_bytes(shape) bytes (scratch).
  * The per-expert counts are recounted from ids rather than taken as an input:
- * a stable order needs the counts of every block of 256 assignments, which
- * the grouping computes anyway, and their sums are the per-expert counts. */
+ * a stable order needs the per-expert counts of every block of assignments,
+ * which the grouping computes anyway, and their sums are the per-expert
+ * counts. */
 MOE_API moe_status moe_permute(const moe_shape* shape, const moe_bf16* x,
                        const int32_t* ids, int32_t* offsets, int32_t* perm_src,
                        int32_t* slot_row, moe_bf16* x_perm, void* ws,
